@@ -1,0 +1,530 @@
+"""Benchmark of the vocab-parallel logits gather on one GB300 (or N replicas).
+
+Default workload (one "step" = one hg_gather call over all TP virtual ranks):
+the decode gather, TP=8 virtual ranks, shard 20480 bf16 columns (40 KB per
+rank-row), V=163840, cap=8, M=1, back-to-back calls on one stream; logits
+bf16(N(0, 3^2)) with 0.1 % sentinel words, seed 1. Inputs and outputs rotate
+over enough sets that one pass touches more bytes than L2 holds, so every call
+reads its shards and writes its outputs cold; the mailboxes are the method's
+own persistent state.
+
+Prints one JSON line (rank 0). Besides the step metric it carries:
+  per_m        us/call at M = 1..8 (TP8, V=163840, cap 8)
+  large_m      us/call, algorithmic GB/s and fraction of the measured HBM peak
+               at M = 64, 128, 256 (TP8, V=163840, cap = M)
+  roofline     the gather kernel on the step workload
+  e2e          the same metric with pinned host buffers, H2D + gather + D2H
+  cpu_baseline the CPU oracle on a bounded sample of the step workload
+  clocks       SM clocks sampled by nvidia-smi around the timed region
+
+--impl reference times the CPU oracle (the reference arm of this build).
+--sweep prints one line per point of the bandwidth sweep instead.
+Multi-GPU: replicas only (one independent gather per GPU; no collective on
+the data path); value = total calls / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "gather µs/call at TP8 V=163840 M=1..8; HBM GB/s and % of peak at large M"
+TP, W, CAP, M_STEP = 8, 20480, 8, 1
+V = TP * W
+SEED = 1
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SRC = os.path.join(ROOT, "tp_vocab_logits_gb300", "csrc", "hg_gather_kernel.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gather_traffic.json")
+
+
+def algorithmic_bytes(tp: int, W: int, M: int) -> int:
+    """Bytes the method must move per call: shard read (M*V*2), push into tp
+    mailboxes, poll read, output write and re-arm write (tp*M*V*2 each)."""
+    Vv = tp * W
+    return M * Vv * 2 * (1 + 4 * tp)
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------- distributed --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(dist, value: float, device) -> float:
+    """Largest value over the ranks (a control-plane reduction of one float)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and getattr(device, "type", "cpu") == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# -------------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, cuda_index: int):
+        self.gpu = self._smi_id(cuda_index)
+        self.proc = None
+        self.path = None
+        self.t_start = self.t_stop = None
+
+    @staticmethod
+    def _smi_id(cuda_index: int) -> str:
+        """nvidia-smi's id of a CUDA device: its UUID (nvidia-smi ignores
+        CUDA_VISIBLE_DEVICES, so the CUDA index is not its index)."""
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            parts = [p for p in vis.split(",") if p.strip()]
+            return parts[cuda_index] if cuda_index < len(parts) else str(cuda_index)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# -------------------------------------------------------------------- timing --
+
+def time_calls(torch, fns, steps: int, warmup: int, stream, flush=None) -> float:
+    """Milliseconds for `steps` calls (fns rotate), CUDA events on `stream`,
+    synchronised on both sides; `warmup` untimed calls first."""
+    for i in range(warmup):
+        fns[i % len(fns)]()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fns[i % len(fns)]()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def make_workload(torch, hg, synth, tp, W, cap, M, sets, device, rows=None, seed=SEED,
+                  dist_kind="normal", scale=3.0, sent=0.001, **create_kw):
+    h = hg.hg_create(tp, W, cap, rows, **create_kw)
+    shards = torch.empty((sets, tp, M, W), dtype=torch.int16, device=device)
+    for s in range(sets):
+        shards[s] = synth.shards(seed, tp, M, W, dist=dist_kind, scale=scale, sent_frac=sent,
+                                 set_index=s % 2000, device=device)
+    outs = torch.empty((sets, tp, M, tp * W), dtype=torch.int16, device=device)
+    calls = [hg.GatherCall(h, [shards[s, r] for r in range(tp)],
+                           [outs[s, d] for d in range(tp)], M) for s in range(sets)]
+    return h, shards, outs, calls
+
+
+def sets_for(tp, W, M, minimum=3) -> int:
+    per = M * tp * W * 2 * (1 + tp)  # shard + output bytes of one set
+    return max(minimum, -(-2 * L2_BYTES // per))
+
+
+def traffic_from_profile(workload_key: str):
+    """Per-launch DRAM bytes of the gather kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    with open(KERNEL_SRC, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if d.get("kernel_sha256_16") != h:
+        return None
+    return d.get("per_launch_dram_bytes", {}).get(workload_key)
+
+
+# ---------------------------------------------------------------- cpu oracle --
+
+def oracle_calls_per_sample(seconds: float):
+    """The CPU oracle on config-2 calls for about `seconds`: (us/call, calls)."""
+    import numpy as np
+
+    import oracle
+    from tp_vocab_logits_gb300 import synth
+    oracle.build()
+    g = oracle.Gather(TP, W, CAP)
+    sets = [synth.shards(SEED, TP, M_STEP, W, scale=3.0, sent_frac=0.001, set_index=i)
+            .numpy().view(np.uint16) for i in range(3)]
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        g.call(sets[n % 3])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return el / n * 1e6, n
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from tp_vocab_logits_gb300 import synth
+    oracle.build()
+    g = oracle.Gather(TP, W, CAP)
+    sets = [synth.shards(SEED, TP, M_STEP, W, scale=3.0, sent_frac=0.001, set_index=i)
+            .numpy().view(np.uint16) for i in range(3)]
+    for i in range(args.warmup):
+        g.call(sets[i % 3])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        g.call(sets[i % 3])
+    el = time.perf_counter() - t0
+    us = el / args.steps * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us/call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1000, 6), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": round(us, 3), "unit": "us/call", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} full config-2 calls (TP8, V=163840, M=1) "
+                                   f"through the single-threaded C++ oracle"},
+        "e2e": {"value": round(us, 3), "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(extra=None) -> dict:
+    c = {"workload": "decode logits gather, TP=8 virtual ranks on one GPU, shard 20480 bf16 "
+                     "(40 KB per rank-row), V=163840, cap=8, M=1, back-to-back calls on one "
+                     "stream; bf16(N(0,9)) logits with 0.1% sentinel words, seed 1",
+         "tp": TP, "shard_cols": W, "V": V, "M": M_STEP, "cap": CAP, "parallelism": "replicas"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# --------------------------------------------------------------------- ours --
+
+def run_ours(args):
+    import torch
+
+    from tp_vocab_logits_gb300 import _build, hg, synth
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    if rank == 0:
+        _build.build()
+    barrier(dist, device)
+    hg.load()
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    # ---- step workload: config 2 ----
+    nsets = sets_for(TP, W, M_STEP)
+    h, shards, outs, calls = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device)
+    ctas, threads = hg.hg_launch_shape(h, M_STEP)
+    # correctness of the timed configuration, untimed: every set once
+    for c in calls:
+        c()
+    hg.hg_sync(h)
+    for s in range(nsets):
+        want = torch.cat([shards[s, r].view(torch.int32) for r in range(TP)], dim=1)
+        want = torch.where(want == -(1 << 31), torch.zeros_like(want), want)
+        for d in range(TP):
+            if not torch.equal(outs[s, d].view(torch.int32), want):
+                raise SystemExit(f"bench: gather output wrong (set {s}, rank {d})")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(dist, device)
+    for i in range(args.warmup):
+        calls[i % nsets]()
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    ms = time_calls(torch, calls, args.steps, 0, stream)
+    hg.hg_sync(h)
+    # keep the same load for a moment so that the clock samples cover it
+    t_end = time.perf_counter() + 0.3
+    while time.perf_counter() < t_end:
+        for i in range(200):
+            calls[i % nsets]()
+        torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms_max = reduce_max(dist, ms, device)
+    us_call = ms_max * 1000.0 / (args.steps * world)
+    us_launch = ms * 1000.0 / args.steps  # this rank's average launch duration
+
+    # ---- e2e: pinned host buffers, H2D + gather + D2H per step ----
+    host_in = [torch.empty((TP, M_STEP, W), dtype=torch.int16).pin_memory() for _ in range(3)]
+    for s in range(3):
+        host_in[s].copy_(shards[s].cpu())
+    host_out = torch.empty((TP, M_STEP, V), dtype=torch.int16).pin_memory()
+    dev_in = torch.empty((TP, M_STEP, W), dtype=torch.int16, device=device)
+    dev_out = torch.empty((TP, M_STEP, V), dtype=torch.int16, device=device)
+    e2e_call = hg.GatherCall(h, [dev_in[r] for r in range(TP)], [dev_out[d] for d in range(TP)],
+                             M_STEP)
+
+    def e2e_step(i=[0]):
+        dev_in.copy_(host_in[i[0] % 3], non_blocking=True)
+        e2e_call()
+        host_out.copy_(dev_out, non_blocking=True)
+        i[0] += 1
+
+    e2e_ms = time_calls(torch, [e2e_step], args.steps, args.warmup, stream)
+    hg.hg_sync(h)
+    want = torch.cat([host_in[(args.warmup + args.steps - 1) % 3][r].view(torch.int32)
+                      for r in range(TP)], dim=1)
+    want = torch.where(want == -(1 << 31), torch.zeros_like(want), want)
+    if not torch.equal(host_out[0].view(torch.int32), want):
+        raise SystemExit("bench: e2e output wrong")
+    e2e_ms_max = reduce_max(dist, e2e_ms, device)
+    h.close()
+    del shards, outs, calls
+
+    # ---- per-M (config 3 row counts) and large M ----
+    per_m = {}
+    if not args.quick:
+        for M in range(1, 9):
+            n = sets_for(TP, W, M)
+            hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, CAP, M, n, device, seed=2)
+            t = time_calls(torch, cm_, 200, 20, stream)
+            hg.hg_sync(hm)
+            per_m[str(M)] = round(t * 1000.0 / 200, 3)
+            hm.close()
+            del sm_, om_, cm_
+    large = {}
+    for M in ([] if args.quick else [64, 128, 256]):
+        hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, M, M, 3, device, seed=3,
+                                          dist_kind="uniform", scale=20.0, sent=0.0)
+        reps = 30
+        t = time_calls(torch, cm_, reps, 5, stream)
+        hg.hg_sync(hm)
+        us = t * 1000.0 / reps
+        gbs = algorithmic_bytes(TP, W, M) / (us * 1e-6) / 1e9
+        c_, t_ = hg.hg_launch_shape(hm, M)
+        large[str(M)] = {"us_per_call": round(us, 2), "algorithmic_GBps": round(gbs, 1),
+                         "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 3),
+                         "ctas": c_, "threads": t_,
+                         "useful_out_GBps": round(TP * M * V * 2 / (us * 1e-6) / 1e9, 1)}
+        hm.close()
+        del sm_, om_, cm_
+
+    # ---- stock cudaMemcpy2D concat baseline on the step workload ----
+    stock_us = None
+    if not args.quick:
+        sb = torch.empty((3, TP, M_STEP, W), dtype=torch.int16, device=device)
+        ob = torch.empty((3, TP, M_STEP, V), dtype=torch.int16, device=device)
+        lib = hg.load()
+        import ctypes
+        arrs = [((ctypes.c_void_p * TP)(*[sb[s, r].data_ptr() for r in range(TP)]),
+                 (ctypes.c_void_p * TP)(*[ob[s, d].data_ptr() for d in range(TP)]))
+                for s in range(3)]
+        sp = stream.cuda_stream
+        fns = [lambda a=a: lib.hg_stock_gather(TP, W, a[0], a[1], M_STEP, sp) for a in arrs]
+        t = time_calls(torch, fns, 200, 20, stream)
+        stock_us = round(t * 1000.0 / 200, 3)
+
+    # ---- CPU oracle on a bounded sample ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        us_cpu, n_cpu = oracle_calls_per_sample(args.cpu_seconds)
+        cpu = {"value": round(us_cpu, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+               "sample": f"{n_cpu} config-2 calls (TP8, V=163840, M=1) through the "
+                         f"single-threaded C++ oracle, {args.cpu_seconds:.0f} s budget"}
+
+    if rank != 0:
+        return 0
+    B = algorithmic_bytes(TP, W, M_STEP)
+    achieved = B / (us_launch * 1e-6) / 1e9
+    traffic = traffic_from_profile("tp8_w20480_m1")
+    line = {
+        "metric": METRIC, "value": round(us_call, 3), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": workload_config({
+            "l2": f"inputs+outputs rotate over {nsets} sets "
+                  f"({nsets * TP * M_STEP * W * 2 * (1 + TP) / 2**20:.0f} MiB > 129 MB L2); "
+                  "mailboxes (42 MB) are the method's persistent state",
+            "launch": {"ctas": ctas, "threads": threads, "cooperative": True}}),
+        "gpu_launches": args.steps,
+        "e2e": {"value": round(e2e_ms_max * 1000.0 / (args.steps * world), 3), "unit": "us/call",
+                "h2d_bytes_per_step": TP * M_STEP * W * 2,
+                "d2h_bytes_per_step": TP * M_STEP * V * 2},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": traffic,
+                     "note": f"algorithmic bytes M*V*2*(1+4*TP) = {B} per launch; peak is the "
+                             f"{pk['source']} HBM copy bandwidth; at M=1 the working set is "
+                             "L2-resident and the launch is latency-bound"},
+        "per_m": per_m,
+        "large_m": large,
+        "stock_memcpy2d_us_per_call": stock_us,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+# -------------------------------------------------------------------- sweep --
+
+def run_sweep(args):
+    import torch
+
+    from tp_vocab_logits_gb300 import _build, hg, synth
+    _build.build()
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    tps = [int(x) for x in args.tps.split(",")]
+    widths = [int(x) for x in args.widths.split(",")]
+    ms = [int(x) for x in args.ms.split(",")]
+    for tp in tps:
+        for Wd in widths:
+            for M in ms:
+                n = sets_for(tp, Wd, M, minimum=2)
+                foot = n * M * tp * Wd * 2 * (1 + tp) + 2 * M * tp * tp * Wd * 2
+                if foot > args.max_gb * 2**30:
+                    n = 2
+                h, s_, o_, c_ = make_workload(torch, hg, synth, tp, Wd, M, M, n, device, seed=3,
+                                              dist_kind="uniform", scale=20.0, sent=0.0)
+                t = time_calls(torch, c_, args.calls, 10, stream)
+                hg.hg_sync(h)
+                us = t * 1000.0 / args.calls
+                gbs = algorithmic_bytes(tp, Wd, M) / (us * 1e-6) / 1e9
+                ctas, threads = hg.hg_launch_shape(h, M)
+                print(json.dumps({"sweep": "bandwidth", "tp": tp, "shard_cols": Wd, "M": M,
+                                  "cap": M, "calls": args.calls, "us_per_call": round(us, 3),
+                                  "algorithmic_GBps": round(gbs, 1),
+                                  "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 3),
+                                  "ctas": ctas, "threads": threads, "sets": n}), flush=True)
+                h.close()
+                del s_, o_, c_
+                torch.cuda.empty_cache()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="step workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true", help="bandwidth sweep, one line per point")
+    ap.add_argument("--tps", default="2,4,8,16")
+    ap.add_argument("--widths", default="4096,8192,20480,65536")
+    ap.add_argument("--ms", default="1,8,32,64,128,256")
+    ap.add_argument("--calls", type=int, default=200)
+    ap.add_argument("--max-gb", type=float, default=120.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,178 @@
+/*
+ * hg.h - C ABI of the vocab-parallel LM-head logits gather on a two-parity
+ * Lamport mailbox, for TP virtual ranks on one GPU.
+ *
+ * The operation (vLLM API page
+ * "vllm.models.kimi_k3.nvidia.specialized_decode.runtime.logits_gather",
+ * module docstring and class HeadGather): each of TP ranks holds an [M, W]
+ * BF16 logits shard (W = V / TP vocab columns). Seen as 32-bit words, rank r's
+ * row m is pushed into row m of EVERY rank's mailbox at word columns
+ * r * W / 2 ... (the rank-order layout of NCCL's all-gather). A mailbox word
+ * that has not arrived holds the sentinel, the BF16 pair (+0, -0) = 0x80000000
+ * (low half +0, high half -0); a data word equal to the sentinel is sent as
+ * (+0, +0) = 0x00000000, every other word moves unchanged. Each rank polls its
+ * mailbox row until no sentinel word is left, copies the row to its [M, V]
+ * output and writes the sentinel back (re-arms). Two mailbox parities
+ * alternate per call, so that a push never lands in a row that the previous
+ * call may still be reading.
+ *
+ * On one GPU the TP ranks are virtual: every rank has its own shard, mailbox
+ * and output allocation on the same device, and one kernel launch runs all of
+ * them.
+ *
+ * Conventions for every entry point:
+ *  - Return value: HG_OK (0) or one of the HG_ERR_* codes below.
+ *  - "device pointer": memory of the device that was current at hg_create;
+ *    the caller keeps that device current for every later call.
+ *  - Calls on one handle are not thread-safe; every gather of a handle runs on
+ *    one stream, in call order (the class docstring's one-stream assumption).
+ *  - A call that returns an error other than HG_ERR_TIMEOUT changed nothing:
+ *    neither the parity nor any mailbox nor any output.
+ */
+#ifndef HG_H_
+#define HG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *hg_stream_t;
+
+/* Opaque, library-owned state of one gather: the mailboxes, the parity, the
+ * device status word and the launch shapes. */
+typedef struct hg_handle hg_handle;
+
+enum {
+  HG_OK = 0,
+  HG_ERR_ARG = 1,      /* invalid argument: NULL, misaligned, out of range */
+  HG_ERR_ROWS = 2,     /* row count M not served by this handle (the page's
+                          HeadGather.__call__ "take stock" branch) */
+  HG_ERR_CAPTURE = 3,  /* stream is capturing a CUDA graph (the class
+                          docstring: calls under a graph capture take stock) */
+  HG_ERR_CUDA = 4,     /* a CUDA runtime call failed (allocation, launch) */
+  HG_ERR_TIMEOUT = 5,  /* a poll gave up: some pushed word never arrived */
+  HG_ERR_STATE = 6     /* the handle holds an unrecovered device error;
+                          call hg_rearm before gathering again */
+};
+
+/* Largest TP supported by one handle. */
+#define HG_MAX_TP 32
+
+/* Optional settings of hg_create_ex. Zero in any field selects the default. */
+typedef struct hg_options {
+  uint64_t poll_timeout_ns; /* bound of every poll; default 1e9 (1 s) */
+  int threads;              /* threads per CTA of the gather kernel: 128, 256,
+                               512 or 1024; default chosen per row count */
+  int ctas;                 /* CTAs of the gather kernel; default chosen per
+                               row count; clamped to what is co-resident */
+} hg_options;
+
+/*
+ * hg_create - allocate and arm the mailboxes of one gather
+ * (HeadGather.__init__: LamportRows(group, device, (2, cap, words * tp),
+ * PAIR_SENT), parity = 0, device synchronised before returning).
+ *
+ *   tp          virtual ranks, 1 <= tp <= HG_MAX_TP
+ *   shard_cols  W, BF16 columns per rank; even (W % 8 == 0 selects the 16-byte
+ *               vector path, other even W a 4-byte word path)
+ *   cap         mailbox rows per parity, >= max(rows)
+ *   rows        the served row counts, each in [1, cap] (HeadGather's `rows`);
+ *               NULL with nrows == 0 serves every M in [1, cap]
+ *   out         receives the handle
+ *
+ * Allocates, on the current device, tp mailboxes of 2 * cap * tp * W BF16
+ * each (parity-major, then row, then column) plus a status word, fills every
+ * mailbox word with 0x80000000 and synchronises the device. The handle owns
+ * that memory until hg_destroy. Errors: HG_ERR_ARG (bad sizes, rows out of
+ * range, size overflow), HG_ERR_CUDA (no device, allocation failure).
+ */
+int hg_create(int tp, int shard_cols, int cap, const int *rows, int nrows, hg_handle **out);
+
+/* hg_create with settings; opt may be NULL. Same contract as hg_create. */
+int hg_create_ex(int tp, int shard_cols, int cap, const int *rows, int nrows,
+                 const hg_options *opt, hg_handle **out);
+
+/* Free the mailboxes and the handle; waits for the device first. NULL is a
+ * no-op. Always returns HG_OK unless freeing fails (HG_ERR_CUDA). */
+int hg_destroy(hg_handle *h);
+
+/*
+ * hg_gather - one gather call (HeadGather.__call__ and the kernel of the module
+ * docstring): push, poll, copy, re-arm, for every virtual rank, in one
+ * persistent kernel launch on `stream`. Asynchronous.
+ *
+ *   shard_ptrs  tp device pointers; shard_ptrs[r] is rank r's [M, W] BF16
+ *               shard, row-major, rows contiguous (row stride W); 16-byte
+ *               aligned on the vector path, 4-byte aligned otherwise; read only
+ *   out_ptrs    tp device pointers; out_ptrs[d] is rank d's [M, tp * W] BF16
+ *               output, row-major, fully overwritten; same alignment rule; must
+ *               not overlap a shard or another output
+ *   M           rows this call; must be a served row count
+ *   stream      the stream every gather of this handle runs on
+ *
+ * Uses parity hg_parity(h), then flips it. The caller owns the shards and the
+ * outputs; the library owns the mailboxes. Errors, all before any device work
+ * and with no parity flip: HG_ERR_ARG (NULL handle or pointer, misaligned
+ * pointer), HG_ERR_ROWS (M not served), HG_ERR_CAPTURE (stream capturing),
+ * HG_ERR_CUDA (launch failed; parity not flipped). A poll that times out on the
+ * device is reported by the next hg_sync; until hg_rearm every later gather
+ * of the handle does no device work.
+ */
+int hg_gather(hg_handle *h, const void *const *shard_ptrs, void *const *out_ptrs, int M,
+              hg_stream_t stream);
+
+/* Wait for `stream`, then read the device status word. Returns HG_OK,
+ * HG_ERR_TIMEOUT (a poll gave up; mailbox contents undefined until hg_rearm)
+ * or HG_ERR_CUDA. */
+int hg_sync(hg_handle *h, hg_stream_t stream);
+
+/* Recovery after an error (the mailbox is the only state besides the parity):
+ * refill every mailbox word of both parities with the sentinel, clear the
+ * status word and set the parity to 0, on `stream`, asynchronously. */
+int hg_rearm(hg_handle *h, hg_stream_t stream);
+
+/* Parity the next hg_gather uses (0 or 1; starts at 0, flips per served call
+ * as `self.parity ^= 1` in HeadGather.__call__), or -1 for NULL. */
+int hg_parity(const hg_handle *h);
+
+/* Rank `rank`'s mailbox for inspection: device pointer to [2][cap][tp * W]
+ * BF16 (parity-major) and its size in bytes. Owned by the handle; read it only
+ * while no gather is in flight. Errors: HG_ERR_ARG. */
+int hg_mailbox(const hg_handle *h, int rank, const void **dev_ptr, size_t *bytes);
+
+/* Launch shape that hg_gather uses for row count M (CTAs, threads per CTA).
+ * Errors: HG_ERR_ARG, HG_ERR_ROWS. */
+int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads);
+
+/*
+ * Test hook for failure detection: make rank `rank`'s push skip its rows in
+ * every later gather (rank = -1 turns it off). The pollers of the other ranks
+ * then wait for words that never arrive and give up after the poll bound;
+ * hg_sync reports HG_ERR_TIMEOUT. No device fault, trap or endless wait is
+ * involved. Errors: HG_ERR_ARG.
+ */
+int hg_debug_skip_push(hg_handle *h, int rank);
+
+/*
+ * hg_stock_gather - the baseline without a mailbox: the rank-order concat of
+ * NCCL's all-gather (the page's stock LogitsProcessor gather: all-gather into
+ * [TP, M, V / TP], then a copy to [M, V]) done as tp * tp cudaMemcpy2DAsync
+ * copies on `stream`. Moves every word unchanged (no sentinel rewrite).
+ * Pointers and layouts as in hg_gather (no alignment rule beyond 2 bytes).
+ * Errors: HG_ERR_ARG, HG_ERR_CUDA.
+ */
+int hg_stock_gather(int tp, int shard_cols, const void *const *shard_ptrs,
+                    void *const *out_ptrs, int M, hg_stream_t stream);
+
+/* Human-readable text of a status code; never NULL. */
+const char *hg_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HG_H_ */

@@ -1,0 +1,283 @@
+"""Parity of the CUDA gather (through the C ABI) with the CPU oracle.
+
+Bit-exact bar: every output word and, after every call, every mailbox word
+of both parities (which must all be the sentinel again) match the oracle;
+the parity sequence matches too. Inputs come from the seeded generator with
+sentinel, (+0,+0) and (-0,-0) words injected, at the pages' workload shapes
+(TP8, 20480-column shards = 40 KB per rank-row, V = 163840, decode row
+counts) and at small shapes that span several units and a ragged tail.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tp_vocab_logits_gb300 import hg, synth
+
+from helpers import S_I32, assert_mailboxes_armed, empty_outs, from_dev, rewrite_concat, to_dev
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from tp_vocab_logits_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+def run_sequence(tp, W, cap, Ms, *, rows=None, seed=7, check_mailbox_every=1, v_real=None,
+                 dist="normal", scale=3.0, sent=0.02, zero=0.01, negzero=0.01, **create_kw):
+    """Gather a sequence of row counts on the GPU and in the oracle; compare
+    outputs word for word, mailboxes and parity after each call."""
+    h = hg.hg_create(tp, W, cap, rows, **create_kw)
+    og = oracle.Gather(tp, W, cap, rows)
+    V = tp * W
+    for i, M in enumerate(Ms):
+        bits = synth.shards(seed, tp, M, W, dist=dist, scale=scale, sent_frac=sent,
+                            zero_frac=zero, negzero_frac=negzero, set_index=i % 2000,
+                            v_real=v_real).numpy().view(np.uint16)
+        want = og.call(bits)
+        shards = to_dev(bits)
+        outs = empty_outs(tp, M, V)
+        assert hg.hg_parity(h) == og.parity ^ 1  # oracle already flipped
+        hg.hg_gather(h, shards, outs, M)
+        hg.hg_sync(h)
+        assert hg.hg_parity(h) == og.parity
+        got = from_dev(outs)
+        if not np.array_equal(got, want):
+            bad = np.argwhere(got != want)
+            raise AssertionError(f"call {i} (M={M}): {len(bad)} words differ, first at {bad[:5]}")
+        if check_mailbox_every and (i % check_mailbox_every == 0 or i == len(Ms) - 1):
+            assert_mailboxes_armed(h, hg)
+    h.close()
+
+
+def test_config1_tiny_golden():
+    """TP=2, V=128, cap=4, M=1, three calls (parity 0, 1, 0) against the stored
+    oracle values of tests/golden/config1_tiny.json."""
+    with open(os.path.join(HERE, "golden", "config1_tiny.json")) as f:
+        gd = json.load(f)
+    tp, W, cap = gd["tp"], gd["shard_cols"], gd["cap"]
+    h = hg.hg_create(tp, W, cap)
+    for c in gd["calls"]:
+        shards_w = np.array([[[int(x, 16) for x in row] for row in r] for r in c["shards"]],
+                            dtype=np.uint32)
+        want = np.array([[[int(x, 16) for x in row] for row in r] for r in c["out"]],
+                        dtype=np.uint32)
+        assert hg.hg_parity(h) == c["parity_before"]
+        outs = empty_outs(tp, 1, tp * W)
+        hg.hg_gather(h, to_dev(shards_w.view(np.uint16).reshape(tp, 1, W)), outs, 1)
+        hg.hg_sync(h)
+        np.testing.assert_array_equal(from_dev(outs).view(np.uint32), want)
+        assert hg.hg_parity(h) == c["parity_after"]
+        assert_mailboxes_armed(h, hg)
+    h.close()
+
+
+@pytest.mark.parametrize("tp,W,cap,Ms", [
+    (2, 64, 4, [1, 1, 1]),             # config 1 shape
+    (2, 8, 1, [1] * 5),                # one vector per rank-row
+    (2, 4, 2, [1, 2, 2, 1]),           # V=8: word path (W % 8 != 0)
+    (3, 6, 3, [3, 1, 2, 3]),           # odd TP, word path
+    (4, 72, 5, [5, 4, 1, 3]),          # ragged: 9 vectors per rank-row
+    (5, 1000, 3, [3, 2, 1]),           # generic-TP kernel, ragged tail of a 128-unit
+    (1, 16, 2, [2, 1, 2]),             # degenerate TP=1
+    (8, 1002, 4, [4, 1, 3]),           # word path, 501 words per rank-row
+    (16, 4096, 4, [4, 1, 2]),          # TP16 vector path
+    (8, 20480, 8, [1, 2, 3, 4, 5, 8, 8, 1]),  # decode shapes, both parities reused
+])
+def test_parity_vs_oracle(tp, W, cap, Ms):
+    run_sequence(tp, W, cap, Ms)
+
+
+@pytest.mark.parametrize("threads,ctas", [(128, 1), (128, 3), (256, 7), (512, 2), (128, 0)])
+def test_launch_shapes_vs_oracle(threads, ctas):
+    """Forced small grids make every CTA loop over many units (and a single CTA
+    consume its own pushes one iteration later)."""
+    run_sequence(4, 2048, 6, [6, 1, 5, 6], threads=threads, ctas=ctas)
+
+
+def test_config2_decode_m1():
+    """TP8, V=163840, cap=8, M=1, back-to-back calls on one stream with 0.1 %
+    sentinel words; every call against the oracle, rotating input sets."""
+    tp, W, cap = 8, 20480, 8
+    h = hg.hg_create(tp, W, cap)
+    og = oracle.Gather(tp, W, cap)
+    sets = [synth.shards(1, tp, 1, W, scale=3.0, sent_frac=0.001, set_index=i)
+            .numpy().view(np.uint16) for i in range(3)]
+    dev = [to_dev(s) for s in sets]
+    outs = empty_outs(tp, 1, tp * W)
+    for i in range(60):
+        want = og.call(sets[i % 3])
+        hg.hg_gather(h, dev[i % 3], outs, 1)
+        if i % 10 == 9 or i < 3:
+            hg.hg_sync(h)
+            np.testing.assert_array_equal(from_dev(outs), want)
+    hg.hg_sync(h)
+    np.testing.assert_array_equal(from_dev(outs), want)
+    assert_mailboxes_armed(h, hg)
+    h.close()
+
+
+def test_config3_speculative_padded_vocab():
+    """TP8, real vocab 163837 padded to 163840 (pads = bf16 -inf), a seeded
+    sequence of row counts over {1,2,3,4,5,8}, cap 8; outputs sliced after."""
+    tp, W, cap, v_real = 8, 20480, 8, 163837
+    rows = [1, 2, 3, 4, 5, 8]
+    Ms = synth.row_sequence(2, 40, rows)
+    h = hg.hg_create(tp, W, cap, rows)
+    og = oracle.Gather(tp, W, cap, rows)
+    for i, M in enumerate(Ms):
+        bits = synth.shards(2, tp, M, W, scale=3.0, set_index=i, v_real=v_real) \
+            .numpy().view(np.uint16)
+        want = og.call(bits)
+        outs = empty_outs(tp, M, tp * W)
+        hg.hg_gather(h, to_dev(bits), outs, M)
+        hg.hg_sync(h)
+        got = from_dev(outs)
+        np.testing.assert_array_equal(got, want)
+        assert (got[:, :, v_real:] == 0xFF80).all()
+        sliced = outs[3][:, :v_real]
+        np.testing.assert_array_equal(sliced.cpu().numpy().view(np.uint16),
+                                      oracle.slice_vocab(want[3], v_real))
+    assert_mailboxes_armed(h, hg)
+    h.close()
+
+
+@pytest.mark.parametrize("tp,W,M", [(2, 4096, 64), (4, 8192, 32), (8, 20480, 8),
+                                    (2, 65536, 8)])
+def test_config4_small_points_vs_oracle(tp, W, M):
+    """Bandwidth-sweep points the oracle finishes quickly, cap = M, U(-20, 20)."""
+    run_sequence(tp, W, M, [M, M, M], dist="uniform", scale=20.0, sent=0.0, zero=0.0,
+                 negzero=0.0, seed=3)
+
+
+@pytest.mark.parametrize("tp,W,M", [(8, 20480, 64), (8, 20480, 256), (16, 65536, 64),
+                                    (16, 4096, 256), (4, 65536, 128)])
+def test_config4_large_points_properties(tp, W, M):
+    """Full-size sweep points: every output equals the rank-order concat with
+    sentinel words sent as zero (the definition's property at any size), and
+    every mailbox is re-armed, over three calls (both parities)."""
+    h = hg.hg_create(tp, W, M)
+    outs = empty_outs(tp, M, tp * W)
+    for i in range(3):
+        bits = synth.shards(3, tp, M, W, dist="uniform", scale=20.0, sent_frac=0.001,
+                            set_index=i, device="cuda")
+        shards = [bits[r] for r in range(tp)]
+        hg.hg_gather(h, shards, outs, M)
+        hg.hg_sync(h)
+        want = rewrite_concat(shards)
+        for d in range(tp):
+            assert torch.equal(outs[d].view(torch.int32), want), f"call {i} rank {d}"
+        assert not any((o.view(torch.int32) == S_I32).any().item() for o in outs)
+    assert_mailboxes_armed(h, hg)
+    h.close()
+
+
+def test_stock_baseline_matches_concat():
+    """The cudaMemcpy2D baseline is the plain concat; without sentinel words it
+    equals the gather bit for bit."""
+    tp, W, M = 8, 20480, 4
+    bits = synth.shards(5, tp, M, W, scale=3.0).numpy().view(np.uint16)
+    shards = to_dev(bits)
+    a = empty_outs(tp, M, tp * W)
+    b = empty_outs(tp, M, tp * W)
+    hg.hg_stock_gather(shards, a, M)
+    h = hg.hg_create(tp, W, 8)
+    hg.hg_gather(h, shards, b, M)
+    hg.hg_sync(h)
+    cat = np.concatenate([bits[r] for r in range(tp)], axis=1)
+    for d in range(tp):
+        np.testing.assert_array_equal(a[d].cpu().numpy().view(np.uint16), cat)
+        assert torch.equal(a[d], b[d])
+    h.close()
+
+
+def test_rejected_calls_change_nothing():
+    """Unserved row counts (M = 0, M > cap, M not in rows), misaligned or
+    missing pointers and graph capture are refused before any device work:
+    parity, mailboxes and outputs stay as they were."""
+    tp, W, cap = 4, 64, 4
+    h = hg.hg_create(tp, W, cap, rows=[1, 3])
+    bits = synth.shards(9, tp, 3, W, scale=3.0).numpy().view(np.uint16)
+    shards = to_dev(bits)
+    outs = empty_outs(tp, 3, tp * W)
+    lib = hg.load()
+    sp = hg._ptr_array(shards)
+    op = hg._ptr_array(outs)
+    stream = torch.cuda.current_stream().cuda_stream
+    for M in (0, 2, 4, 5, -1):
+        assert lib.hg_gather(h.ptr, sp, op, M, stream) == hg.HG_ERR_ROWS
+    # misaligned output pointer (2 bytes off) and a NULL shard pointer
+    import ctypes
+    bad = (ctypes.c_void_p * tp)(*[o.data_ptr() + 2 for o in outs])
+    assert lib.hg_gather(h.ptr, sp, bad, 3, stream) == hg.HG_ERR_ARG
+    nul = (ctypes.c_void_p * tp)(*([None] + [s.data_ptr() for s in shards[1:]]))
+    assert lib.hg_gather(h.ptr, nul, op, 3, stream) == hg.HG_ERR_ARG
+    assert lib.hg_gather(None, sp, op, 3, stream) == hg.HG_ERR_ARG
+    # graph capture: refused, nothing captured
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        st = lib.hg_gather(h.ptr, sp, op, 3, s.cuda_stream)
+        g.capture_end()
+    assert st == hg.HG_ERR_CAPTURE
+    torch.cuda.synchronize()
+    assert hg.hg_parity(h) == 0
+    assert (from_dev(outs) == 0x5A5A).all()
+    assert_mailboxes_armed(h, hg)
+    # a served call still works and is the first use of parity 0
+    og = oracle.Gather(tp, W, cap, [1, 3])
+    hg.hg_gather(h, shards, outs, 3)
+    hg.hg_sync(h)
+    np.testing.assert_array_equal(from_dev(outs), og.call(bits))
+    h.close()
+
+
+def test_create_rejects_bad_sizes():
+    for args in [(0, 64, 4), (hg.HG_MAX_TP + 1, 64, 4), (2, 7, 4), (2, 0, 4),
+                 (2, 64, 0)]:
+        with pytest.raises(hg.HGError) as e:
+            hg.hg_create(*args)
+        assert e.value.status == hg.HG_ERR_ARG
+    with pytest.raises(hg.HGError):
+        hg.hg_create(2, 64, 4, rows=[5])
+
+
+def test_timeout_recovery():
+    """Failure detection without a GPU fault: rank 3's push is skipped (host
+    test hook), the other ranks' polls give up after 20 ms, hg_sync reports
+    the timeout, later calls are refused until hg_rearm, and after re-arming
+    the gather is exact again."""
+    tp, W, cap = 8, 4096, 2
+    h = hg.hg_create(tp, W, cap, poll_timeout_ns=20_000_000)
+    bits = synth.shards(6, tp, 2, W, scale=3.0, sent_frac=0.01).numpy().view(np.uint16)
+    shards = to_dev(bits)
+    outs = empty_outs(tp, 2, tp * W)
+    hg.hg_debug_skip_push(h, 3)
+    hg.hg_gather(h, shards, outs, 2)
+    with pytest.raises(hg.HGError) as e:
+        hg.hg_sync(h)
+    assert e.value.status == hg.HG_ERR_TIMEOUT
+    with pytest.raises(hg.HGError) as e:
+        hg.hg_gather(h, shards, outs, 2)
+    assert e.value.status == hg.HG_ERR_STATE
+    hg.hg_debug_skip_push(h, -1)
+    hg.hg_rearm(h)
+    assert hg.hg_parity(h) == 0
+    assert_mailboxes_armed(h, hg)
+    og = oracle.Gather(tp, W, cap)
+    for _ in range(3):
+        want = og.call(bits)
+        hg.hg_gather(h, shards, outs, 2)
+        hg.hg_sync(h)
+        np.testing.assert_array_equal(from_dev(outs), want)
+    assert_mailboxes_armed(h, hg)
+    h.close()

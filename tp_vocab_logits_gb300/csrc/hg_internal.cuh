@@ -1,0 +1,49 @@
+// Internal declarations shared by the gather library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "hg.h"
+
+namespace hg {
+
+// Sentinel word: the BF16 pair (+0, -0), +0 in the low half (column 2k), -0 in
+// the high half (column 2k+1); a data word equal to it is sent as (+0, +0).
+// (vLLM API page "...runtime.logits_gather", module docstring.)
+constexpr uint32_t kSentinel = 0x80000000u;
+constexpr uint32_t kSentAs = 0x00000000u;
+
+// Device status word values (status[0]); status[1..3] record where a poll
+// gave up: unit index, consumer rank, first word offset.
+enum DevStatus : int { kDevOk = 0, kDevTimeout = 1 };
+constexpr int kStatusWords = 4;
+
+// Arguments of one gather launch. Element = 16-byte vector (vector path) or
+// one 32-bit word (word path).
+struct GatherArgs {
+  const void* shard[HG_MAX_TP];  // rank r's [M][wv] elements
+  void* out[HG_MAX_TP];          // rank d's [M][tp * wv] elements
+  void* box[HG_MAX_TP];          // rank d's mailbox, parity in use: [cap][tp * wv]
+  int* status;                   // device status words (kStatusWords)
+  unsigned long long timeout_ns;
+  int tp;
+  int wv;         // elements per rank-row
+  int M;          // rows of this call
+  int chunks;     // units per rank-row: ceil(wv / blockDim.x)
+  int skip_rank;  // test hook: rank whose push is skipped (-1: none)
+};
+
+// Largest co-resident CTAs per SM of the gather kernel for this shape.
+cudaError_t gather_occupancy(bool vec16, int tp, int threads, int* ctas_per_sm);
+
+// Cooperative launch of the gather kernel: all `ctas` CTAs co-resident.
+cudaError_t launch_gather(const GatherArgs& a, bool vec16, int ctas, int threads,
+                          cudaStream_t stream);
+
+// Fill n 32-bit words with v.
+cudaError_t launch_fill_u32(uint32_t* p, size_t n, uint32_t v, cudaStream_t stream);
+
+}  // namespace hg

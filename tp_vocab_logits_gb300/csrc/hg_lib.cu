@@ -1,0 +1,288 @@
+// Host side of the C ABI declared in include/hg.h: handle, mailboxes, parity,
+// argument checks, launch shapes and the stock baseline.
+//
+// The per-call logic follows HeadGather (vLLM API page "vllm.models.kimi_k3.
+// nvidia.specialized_decode.runtime.logits_gather"): unserved row counts and
+// graph capture are refused before any state changes (__call__'s eligibility
+// test); otherwise the call uses the current parity, flips it, and launches
+// one kernel.
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "hg_internal.cuh"
+
+struct hg_handle {
+  int device = -1;
+  int sms = 0;
+  int tp = 0;
+  int W = 0;       // shard columns
+  int wv = 0;      // elements per rank-row (16-byte vectors or words)
+  bool vec16 = false;
+  int cap = 0;
+  std::vector<char> served;  // served[M]
+  int parity = 0;
+  size_t box_bytes = 0;      // bytes of one rank's mailbox, both parities
+  size_t parity_elems = 0;   // elements of one parity of one mailbox
+  void* box[HG_MAX_TP] = {};
+  int* status = nullptr;     // device status words
+  unsigned long long timeout_ns = 1000000000ull;
+  int skip_rank = -1;
+  bool failed = false;       // hg_sync saw a device error; cleared by hg_rearm
+  std::vector<int> ctas;     // launch shape per M (index M)
+  std::vector<int> threads;
+  std::vector<int> chunks;
+};
+
+namespace {
+
+using hg::GatherArgs;
+
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+void free_handle(hg_handle* h) {
+  if (!h) return;
+  for (int d = 0; d < HG_MAX_TP; ++d)
+    if (h->box[d]) cudaFree(h->box[d]);
+  if (h->status) cudaFree(h->status);
+  delete h;
+}
+
+// Launch shape for M rows: threads per CTA and CTAs. The unit is one element
+// per thread; the default picks the widest CTA that still gives every SM a
+// unit, so that small row counts spread over the whole GPU, and caps the grid
+// at the co-resident maximum (the kernel's polls need every CTA resident).
+int plan_shapes(hg_handle* h, const hg_options* opt) {
+  h->ctas.assign(h->cap + 1, 0);
+  h->threads.assign(h->cap + 1, 0);
+  h->chunks.assign(h->cap + 1, 0);
+  for (int M = 1; M <= h->cap; ++M) {
+    if (!h->served[M]) continue;
+    int T = opt && opt->threads ? opt->threads : 0;
+    if (T == 0) {
+      T = 128;
+      for (int cand : {512, 256}) {
+        const long long units = (long long)M * h->tp * ((h->wv + cand - 1) / cand);
+        if (units >= h->sms) { T = cand; break; }
+      }
+    }
+    if (T != 128 && T != 256 && T != 512) return HG_ERR_ARG;
+    int per_sm = 0;
+    if (hg::gather_occupancy(h->vec16, h->tp, T, &per_sm) != cudaSuccess || per_sm < 1)
+      return HG_ERR_CUDA;
+    const long long max_g = (long long)per_sm * h->sms;
+    const int chunks = (h->wv + T - 1) / T;
+    const long long units = (long long)M * h->tp * chunks;
+    if (units > 0x7fffffffLL) return HG_ERR_ARG;
+    long long G = opt && opt->ctas ? opt->ctas : units;
+    if (G > max_g) G = max_g;
+    if (G > units) G = units;
+    if (G < 1) G = 1;
+    h->ctas[M] = (int)G;
+    h->threads[M] = T;
+    h->chunks[M] = chunks;
+  }
+  return HG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* hg_strerror(int status) {
+  switch (status) {
+    case HG_OK: return "ok";
+    case HG_ERR_ARG: return "invalid argument";
+    case HG_ERR_ROWS: return "row count not served by this gather";
+    case HG_ERR_CAPTURE: return "stream is capturing a CUDA graph";
+    case HG_ERR_CUDA: return "CUDA runtime error";
+    case HG_ERR_TIMEOUT: return "mailbox poll timed out";
+    case HG_ERR_STATE: return "gather holds an unrecovered device error; re-arm it";
+    default: return "unknown status";
+  }
+}
+
+int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
+                 const hg_options* opt, hg_handle** out) {
+  if (!out) return HG_ERR_ARG;
+  *out = nullptr;
+  if (tp < 1 || tp > HG_MAX_TP || shard_cols < 2 || shard_cols % 2 != 0 || cap < 1)
+    return HG_ERR_ARG;
+  if (nrows < 0 || (nrows > 0 && !rows)) return HG_ERR_ARG;
+  const long long V = (long long)tp * shard_cols;
+  const long long words_per_row = V / 2;
+  if (words_per_row > (1LL << 30) || (long long)cap * words_per_row > (1LL << 40))
+    return HG_ERR_ARG;
+
+  hg_handle* h = new (std::nothrow) hg_handle;
+  if (!h) return HG_ERR_CUDA;
+  h->tp = tp;
+  h->W = shard_cols;
+  h->vec16 = shard_cols % 8 == 0;
+  h->wv = h->vec16 ? shard_cols / 8 : shard_cols / 2;
+  h->cap = cap;
+  h->served.assign(cap + 1, 0);
+  if (nrows == 0) {
+    for (int m = 1; m <= cap; ++m) h->served[m] = 1;
+  } else {
+    for (int i = 0; i < nrows; ++i) {
+      if (rows[i] < 1 || rows[i] > cap) { delete h; return HG_ERR_ARG; }
+      h->served[rows[i]] = 1;
+    }
+  }
+  h->timeout_ns = opt && opt->poll_timeout_ns ? opt->poll_timeout_ns : kDefaultTimeoutNs;
+
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return HG_ERR_CUDA;
+  }
+  int coop = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
+  if (!coop) { delete h; return HG_ERR_CUDA; }
+
+  int st = plan_shapes(h, opt);
+  if (st != HG_OK) { delete h; return st; }
+
+  // Mailboxes: [2 parities][cap rows][V] bf16 per rank, armed with the sentinel.
+  const size_t row_bytes = (size_t)V * 2;
+  h->box_bytes = 2 * (size_t)cap * row_bytes;
+  h->parity_elems = (size_t)cap * tp * h->wv;
+  for (int d = 0; d < tp; ++d) {
+    if (cudaMalloc(&h->box[d], h->box_bytes) != cudaSuccess) { free_handle(h); return HG_ERR_CUDA; }
+    if (hg::launch_fill_u32(static_cast<uint32_t*>(h->box[d]), h->box_bytes / 4, hg::kSentinel,
+                            nullptr) != cudaSuccess) {
+      free_handle(h);
+      return HG_ERR_CUDA;
+    }
+  }
+  if (cudaMalloc(&h->status, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
+      cudaMemset(h->status, 0, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    free_handle(h);
+    return HG_ERR_CUDA;
+  }
+  *out = h;
+  return HG_OK;
+}
+
+int hg_create(int tp, int shard_cols, int cap, const int* rows, int nrows, hg_handle** out) {
+  return hg_create_ex(tp, shard_cols, cap, rows, nrows, nullptr, out);
+}
+
+int hg_destroy(hg_handle* h) {
+  if (!h) return HG_OK;
+  int st = cudaDeviceSynchronize() == cudaSuccess ? HG_OK : HG_ERR_CUDA;
+  free_handle(h);
+  return st;
+}
+
+int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
+              hg_stream_t stream) {
+  if (!h || !shard_ptrs || !out_ptrs) return HG_ERR_ARG;
+  if (M < 1 || M > h->cap || !h->served[M]) return HG_ERR_ROWS;
+  if (h->failed) return HG_ERR_STATE;
+  const size_t align = h->vec16 ? 16 : 4;
+  GatherArgs a;
+  for (int r = 0; r < h->tp; ++r) {
+    if (!shard_ptrs[r] || !out_ptrs[r] || !aligned(shard_ptrs[r], align) ||
+        !aligned(out_ptrs[r], align))
+      return HG_ERR_ARG;
+    a.shard[r] = shard_ptrs[r];
+    a.out[r] = out_ptrs[r];
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return HG_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return HG_ERR_CAPTURE;
+
+  const size_t esz = h->vec16 ? 16 : 4;
+  for (int d = 0; d < h->tp; ++d)
+    a.box[d] = static_cast<char*>(h->box[d]) + (size_t)h->parity * h->parity_elems * esz;
+  for (int d = h->tp; d < HG_MAX_TP; ++d) {
+    a.shard[d] = nullptr;
+    a.out[d] = nullptr;
+    a.box[d] = nullptr;
+  }
+  a.status = h->status;
+  a.timeout_ns = h->timeout_ns;
+  a.tp = h->tp;
+  a.wv = h->wv;
+  a.M = M;
+  a.chunks = h->chunks[M];
+  a.skip_rank = h->skip_rank;
+  if (hg::launch_gather(a, h->vec16, h->ctas[M], h->threads[M], stream) != cudaSuccess)
+    return HG_ERR_CUDA;
+  h->parity ^= 1;
+  return HG_OK;
+}
+
+int hg_sync(hg_handle* h, hg_stream_t stream) {
+  if (!h) return HG_ERR_ARG;
+  int st[hg::kStatusWords] = {};
+  if (cudaMemcpyAsync(st, h->status, sizeof st, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return HG_ERR_CUDA;
+  if (st[0] == hg::kDevOk) return HG_OK;
+  h->failed = true;
+  return HG_ERR_TIMEOUT;
+}
+
+int hg_rearm(hg_handle* h, hg_stream_t stream) {
+  if (!h) return HG_ERR_ARG;
+  for (int d = 0; d < h->tp; ++d)
+    if (hg::launch_fill_u32(static_cast<uint32_t*>(h->box[d]), h->box_bytes / 4, hg::kSentinel,
+                            stream) != cudaSuccess)
+      return HG_ERR_CUDA;
+  if (cudaMemsetAsync(h->status, 0, hg::kStatusWords * sizeof(int), stream) != cudaSuccess)
+    return HG_ERR_CUDA;
+  h->parity = 0;
+  h->failed = false;
+  return HG_OK;
+}
+
+int hg_parity(const hg_handle* h) { return h ? h->parity : -1; }
+
+int hg_mailbox(const hg_handle* h, int rank, const void** dev_ptr, size_t* bytes) {
+  if (!h || rank < 0 || rank >= h->tp || !dev_ptr || !bytes) return HG_ERR_ARG;
+  *dev_ptr = h->box[rank];
+  *bytes = h->box_bytes;
+  return HG_OK;
+}
+
+int hg_launch_shape(const hg_handle* h, int M, int* ctas, int* threads) {
+  if (!h || !ctas || !threads) return HG_ERR_ARG;
+  if (M < 1 || M > h->cap || !h->served[M]) return HG_ERR_ROWS;
+  *ctas = h->ctas[M];
+  *threads = h->threads[M];
+  return HG_OK;
+}
+
+int hg_debug_skip_push(hg_handle* h, int rank) {
+  if (!h || rank < -1 || rank >= h->tp) return HG_ERR_ARG;
+  h->skip_rank = rank;
+  return HG_OK;
+}
+
+int hg_stock_gather(int tp, int shard_cols, const void* const* shard_ptrs, void* const* out_ptrs,
+                    int M, hg_stream_t stream) {
+  if (tp < 1 || tp > HG_MAX_TP || shard_cols < 1 || M < 0 || !shard_ptrs || !out_ptrs)
+    return HG_ERR_ARG;
+  for (int r = 0; r < tp; ++r)
+    if (!shard_ptrs[r] || !out_ptrs[r]) return HG_ERR_ARG;
+  if (M == 0) return HG_OK;
+  const size_t wbytes = (size_t)shard_cols * 2;
+  const size_t vbytes = wbytes * tp;
+  for (int d = 0; d < tp; ++d)
+    for (int r = 0; r < tp; ++r)
+      if (cudaMemcpy2DAsync(static_cast<char*>(out_ptrs[d]) + r * wbytes, vbytes, shard_ptrs[r],
+                            wbytes, wbytes, (size_t)M, cudaMemcpyDeviceToDevice,
+                            stream) != cudaSuccess)
+        return HG_ERR_CUDA;
+  return HG_OK;
+}
+
+}  // extern "C"

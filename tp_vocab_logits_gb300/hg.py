@@ -1,0 +1,237 @@
+"""Python binding of libhg (include/hg.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+computation of its own: it checks torch tensors' device, dtype, shape and
+contiguity, turns them into raw device pointers, and calls the library. The
+gather itself runs only in the library's CUDA kernels; if libhg.so cannot be
+loaded every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+from . import _build
+
+HG_OK, HG_ERR_ARG, HG_ERR_ROWS, HG_ERR_CAPTURE, HG_ERR_CUDA, HG_ERR_TIMEOUT, HG_ERR_STATE = range(7)
+HG_MAX_TP = 32
+
+
+class HGError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {strerror(status)} (status {status})")
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("poll_timeout_ns", ctypes.c_uint64), ("threads", ctypes.c_int),
+                ("ctas", ctypes.c_int)]
+
+
+_LIB: ctypes.CDLL | None = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libhg.so (built in-tree by ``_build.build()``); raises if absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with tp_vocab_logits_gb300._build.build()")
+    lib = ctypes.CDLL(path)
+    vp, vpp, i, st = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_void_p
+    lib.hg_create.argtypes = [i, i, i, ctypes.POINTER(i), i, ctypes.POINTER(vp)]
+    lib.hg_create_ex.argtypes = [i, i, i, ctypes.POINTER(i), i, ctypes.POINTER(_Options),
+                                 ctypes.POINTER(vp)]
+    lib.hg_destroy.argtypes = [vp]
+    lib.hg_gather.argtypes = [vp, vpp, vpp, i, st]
+    lib.hg_sync.argtypes = [vp, st]
+    lib.hg_rearm.argtypes = [vp, st]
+    lib.hg_parity.argtypes = [vp]
+    lib.hg_mailbox.argtypes = [vp, i, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)]
+    lib.hg_launch_shape.argtypes = [vp, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    lib.hg_debug_skip_push.argtypes = [vp, i]
+    lib.hg_stock_gather.argtypes = [i, i, vpp, vpp, i, st]
+    lib.hg_strerror.argtypes = [i]
+    lib.hg_strerror.restype = ctypes.c_char_p
+    for name in ("hg_create", "hg_create_ex", "hg_destroy", "hg_gather", "hg_sync", "hg_rearm",
+                 "hg_parity", "hg_mailbox", "hg_launch_shape", "hg_debug_skip_push",
+                 "hg_stock_gather"):
+        getattr(lib, name).restype = i
+    _LIB = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load().hg_strerror(status).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _check(status: int, where: str) -> None:
+    if status != HG_OK:
+        raise HGError(status, where)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr_array(tensors: Sequence[torch.Tensor]):
+    return (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+class Handle:
+    """Owner of one hg_handle; freed by hg_destroy on close() or collection."""
+
+    def __init__(self, ptr: int, tp: int, shard_cols: int, cap: int, rows):
+        self.ptr = ptr
+        self.tp, self.shard_cols, self.cap = tp, shard_cols, cap
+        self.rows = frozenset(rows) if rows else frozenset(range(1, cap + 1))
+
+    @property
+    def V(self) -> int:
+        return self.tp * self.shard_cols
+
+    def close(self) -> None:
+        if self.ptr:
+            _check(load().hg_destroy(self.ptr), "hg_destroy")
+            self.ptr = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def hg_create(tp: int, shard_cols: int, cap: int, rows: Sequence[int] | None = None, *,
+              poll_timeout_ns: int = 0, threads: int = 0, ctas: int = 0) -> Handle:
+    lib = load()
+    rows = list(rows or [])
+    arr = (ctypes.c_int * max(1, len(rows)))(*rows)
+    out = ctypes.c_void_p()
+    if poll_timeout_ns or threads or ctas:
+        opt = _Options(poll_timeout_ns, threads, ctas)
+        st = lib.hg_create_ex(tp, shard_cols, cap, arr, len(rows), ctypes.byref(opt),
+                              ctypes.byref(out))
+    else:
+        st = lib.hg_create(tp, shard_cols, cap, arr, len(rows), ctypes.byref(out))
+    _check(st, "hg_create")
+    return Handle(out.value, tp, shard_cols, cap, rows)
+
+
+def hg_destroy(h: Handle) -> None:
+    h.close()
+
+
+def _check_tensors(ts: Sequence[torch.Tensor], n: int, cols: int, M: int, what: str) -> None:
+    if len(ts) != n:
+        raise ValueError(f"{what}: expected {n} tensors, got {len(ts)}")
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError(f"{what}: tensors must be on a CUDA device")
+        if t.dtype not in (torch.bfloat16, torch.int16):
+            raise ValueError(f"{what}: dtype must be bfloat16 (or its int16 bits), got {t.dtype}")
+        if tuple(t.shape) != (M, cols) or not t.is_contiguous():
+            raise ValueError(f"{what}: need contiguous [{M}, {cols}], got {tuple(t.shape)}")
+
+
+class GatherCall:
+    """Marshalled arguments of one hg_gather call, reusable across calls with
+    the same buffers (keeps per-call host work to the C call itself)."""
+
+    def __init__(self, h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
+                 M: int, stream=None):
+        _check_tensors(shards, h.tp, h.shard_cols, M, "shards")
+        _check_tensors(outs, h.tp, h.V, M, "outs")
+        self.h, self.M = h, M
+        self._keep = (list(shards), list(outs))
+        self._sp = _ptr_array(shards)
+        self._op = _ptr_array(outs)
+        self._stream = _stream_ptr(stream)
+        self._fn = load().hg_gather
+
+    def __call__(self) -> None:
+        st = self._fn(self.h.ptr, self._sp, self._op, self.M, self._stream)
+        if st != HG_OK:
+            raise HGError(st, "hg_gather")
+
+
+def hg_gather(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
+              M: int | None = None, stream=None) -> None:
+    """One gather: shards[r] is rank r's [M, W] bf16 logits, outs[d] rank d's
+    [M, V] bf16 output (both lists of device tensors)."""
+    M = shards[0].shape[0] if M is None else M
+    GatherCall(h, shards, outs, M, stream)()
+
+
+def hg_sync(h: Handle, stream=None) -> None:
+    _check(load().hg_sync(h.ptr, _stream_ptr(stream)), "hg_sync")
+
+
+def hg_rearm(h: Handle, stream=None) -> None:
+    _check(load().hg_rearm(h.ptr, _stream_ptr(stream)), "hg_rearm")
+
+
+def hg_parity(h: Handle) -> int:
+    return int(load().hg_parity(h.ptr))
+
+
+def hg_mailbox(h: Handle, rank: int) -> tuple:
+    """(device pointer, bytes) of rank's [2, cap, V] bf16 mailbox."""
+    p = ctypes.c_void_p()
+    n = ctypes.c_size_t()
+    _check(load().hg_mailbox(h.ptr, rank, ctypes.byref(p), ctypes.byref(n)), "hg_mailbox")
+    return int(p.value), int(n.value)
+
+
+class _DeviceView:
+    """Read-only view of library-owned device memory for torch.as_tensor."""
+
+    def __init__(self, ptr: int, shape: tuple, typestr: str):
+        self.__cuda_array_interface__ = {"shape": shape, "typestr": typestr,
+                                         "data": (ptr, True), "version": 3, "strides": None}
+
+
+def mailbox_words(h: Handle, rank: int) -> torch.Tensor:
+    """Copy of rank's mailbox as int32 words [2, cap, V / 2] (device tensor).
+    Read it only while no gather of the handle is in flight."""
+    ptr, nbytes = hg_mailbox(h, rank)
+    shape = (2, h.cap, h.V // 2)
+    assert nbytes == 4 * shape[0] * shape[1] * shape[2]
+    view = torch.as_tensor(_DeviceView(ptr, shape, "<i4"), device="cuda")
+    return view.clone()
+
+
+def hg_launch_shape(h: Handle, M: int) -> tuple:
+    c, t = ctypes.c_int(), ctypes.c_int()
+    _check(load().hg_launch_shape(h.ptr, M, ctypes.byref(c), ctypes.byref(t)), "hg_launch_shape")
+    return c.value, t.value
+
+
+def hg_debug_skip_push(h: Handle, rank: int) -> None:
+    _check(load().hg_debug_skip_push(h.ptr, rank), "hg_debug_skip_push")
+
+
+def hg_stock_gather(shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
+                    M: int | None = None, stream=None) -> None:
+    tp = len(shards)
+    M = shards[0].shape[0] if M is None else M
+    W = shards[0].shape[1]
+    _check_tensors(shards, tp, W, M, "shards")
+    _check_tensors(outs, tp, tp * W, M, "outs")
+    _check(load().hg_stock_gather(tp, W, _ptr_array(shards), _ptr_array(outs), M,
+                                  _stream_ptr(stream)), "hg_stock_gather")
