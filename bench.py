@@ -174,19 +174,22 @@ class ClockSampler:
 
 # -------------------------------------------------------------------- timing --
 
-def time_calls(torch, fns, steps: int, warmup: int, stream, flush=None) -> float:
+def time_calls(torch, fns, steps: int, warmup: int, stream, label: str = "timed") -> float:
     """Milliseconds for `steps` calls (fns rotate), CUDA events on `stream`,
-    synchronised on both sides; `warmup` untimed calls first."""
+    synchronised on both sides; `warmup` untimed calls first. The timed calls
+    sit in an NVTX range named `label` (ncu --nvtx-include "<label>/")."""
     for i in range(warmup):
         fns[i % len(fns)]()
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push(label)
     start.record(stream)
     for i in range(steps):
         fns[i % len(fns)]()
     end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     return start.elapsed_time(end)
 
 
@@ -313,7 +316,7 @@ def run_ours(args):
     # ---- step workload: config 2 ----
     nsets = sets_for(TP, W, M_STEP)
     h, shards, outs, calls = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device)
-    ctas, threads = hg.hg_launch_shape(h, M_STEP)
+    shape = hg.hg_launch_shape(h, M_STEP)
     # correctness of the timed configuration, untimed: every set once
     for c in calls:
         c()
@@ -334,7 +337,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(dist, device)
     torch.cuda.synchronize()
-    ms = time_calls(torch, calls, args.steps, 0, stream)
+    ms = time_calls(torch, calls, args.steps, 0, stream, "timed_step")
     hg.hg_sync(h)
     # keep the same load for a moment so that the clock samples cover it
     t_end = time.perf_counter() + 0.3
@@ -363,7 +366,7 @@ def run_ours(args):
         host_out.copy_(dev_out, non_blocking=True)
         i[0] += 1
 
-    e2e_ms = time_calls(torch, [e2e_step], args.steps, args.warmup, stream)
+    e2e_ms = time_calls(torch, [e2e_step], args.steps, args.warmup, stream, "timed_e2e")
     hg.hg_sync(h)
     want = torch.cat([host_in[(args.warmup + args.steps - 1) % 3][r].view(torch.int32)
                       for r in range(TP)], dim=1)
@@ -394,10 +397,9 @@ def run_ours(args):
         hg.hg_sync(hm)
         us = t * 1000.0 / reps
         gbs = algorithmic_bytes(TP, W, M) / (us * 1e-6) / 1e9
-        c_, t_ = hg.hg_launch_shape(hm, M)
         large[str(M)] = {"us_per_call": round(us, 2), "algorithmic_GBps": round(gbs, 1),
                          "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 3),
-                         "ctas": c_, "threads": t_,
+                         "launch": hg.hg_launch_shape(hm, M),
                          "useful_out_GBps": round(TP * M * V * 2 / (us * 1e-6) / 1e9, 1)}
         hm.close()
         del sm_, om_, cm_
@@ -439,7 +441,7 @@ def run_ours(args):
             "l2": f"inputs+outputs rotate over {nsets} sets "
                   f"({nsets * TP * M_STEP * W * 2 * (1 + TP) / 2**20:.0f} MiB > 129 MB L2); "
                   "mailboxes (42 MB) are the method's persistent state",
-            "launch": {"ctas": ctas, "threads": threads, "cooperative": True}}),
+            "launch": dict(shape, launch="programmatic dependent launch")}),
         "gpu_launches": args.steps,
         "e2e": {"value": round(e2e_ms_max * 1000.0 / (args.steps * world), 3), "unit": "us/call",
                 "h2d_bytes_per_step": TP * M_STEP * W * 2,
@@ -484,17 +486,20 @@ def run_sweep(args):
                 if foot > args.max_gb * 2**30:
                     n = 2
                 h, s_, o_, c_ = make_workload(torch, hg, synth, tp, Wd, M, M, n, device, seed=3,
-                                              dist_kind="uniform", scale=20.0, sent=0.0)
+                                              dist_kind="uniform", scale=20.0, sent=0.0,
+                                              elems_per_lane=args.vpt, ctas=args.ctas,
+                                              poll_mode=args.poll_mode,
+                                              cooperative=args.cooperative)
                 t = time_calls(torch, c_, args.calls, 10, stream)
                 hg.hg_sync(h)
                 us = t * 1000.0 / args.calls
                 gbs = algorithmic_bytes(tp, Wd, M) / (us * 1e-6) / 1e9
-                ctas, threads = hg.hg_launch_shape(h, M)
                 print(json.dumps({"sweep": "bandwidth", "tp": tp, "shard_cols": Wd, "M": M,
+                                  "cooperative": args.cooperative,
                                   "cap": M, "calls": args.calls, "us_per_call": round(us, 3),
                                   "algorithmic_GBps": round(gbs, 1),
                                   "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 3),
-                                  "ctas": ctas, "threads": threads, "sets": n}), flush=True)
+                                  "launch": hg.hg_launch_shape(h, M), "sets": n}), flush=True)
                 h.close()
                 del s_, o_, c_
                 torch.cuda.empty_cache()
@@ -516,6 +521,10 @@ def main(argv=None):
     ap.add_argument("--ms", default="1,8,32,64,128,256")
     ap.add_argument("--calls", type=int, default=200)
     ap.add_argument("--max-gb", type=float, default=120.0)
+    ap.add_argument("--vpt", type=int, default=0, help="sweep: force elements per lane")
+    ap.add_argument("--ctas", type=int, default=0, help="sweep: force the CTA count")
+    ap.add_argument("--poll-mode", type=int, default=0, help="sweep: 1 pipelined, 2 simple")
+    ap.add_argument("--cooperative", action="store_true", help="sweep: cooperative launch")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -65,10 +65,17 @@ enum {
 /* Optional settings of hg_create_ex. Zero in any field selects the default. */
 typedef struct hg_options {
   uint64_t poll_timeout_ns; /* bound of every poll; default 1e9 (1 s) */
-  int threads;              /* threads per CTA of the gather kernel: 128, 256,
-                               512 or 1024; default chosen per row count */
-  int ctas;                 /* CTAs of the gather kernel; default chosen per
-                               row count; clamped to what is co-resident */
+  int elems_per_lane;       /* 16-byte vectors (or words) per lane per unit:
+                               1, 2 or 4; default chosen per row count */
+  int ctas;                 /* CTAs of the gather kernel (32 * tp threads each);
+                               default chosen per row count; clamped to what is
+                               co-resident */
+  int poll_mode;            /* 0: by launch shape (pipelined when one wave
+                               covers the call), 1: pipelined, 2: simple */
+  int cooperative;          /* 0 (default): programmatic dependent launch, the
+                               next call's launch overlaps this one; 1:
+                               cooperative launch, the runtime itself checks
+                               that every CTA is co-resident (no overlap) */
 } hg_options;
 
 /*
@@ -144,9 +151,11 @@ int hg_parity(const hg_handle *h);
  * while no gather is in flight. Errors: HG_ERR_ARG. */
 int hg_mailbox(const hg_handle *h, int rank, const void **dev_ptr, size_t *bytes);
 
-/* Launch shape that hg_gather uses for row count M (CTAs, threads per CTA).
- * Errors: HG_ERR_ARG, HG_ERR_ROWS. */
-int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads);
+/* Launch shape that hg_gather uses for row count M: CTAs, threads per CTA,
+ * elements per lane and whether polls are pipelined (1) or simple (0). Any
+ * output pointer may be NULL. Errors: HG_ERR_ARG, HG_ERR_ROWS. */
+int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *elems_per_lane,
+                    int *pipelined);
 
 /*
  * Test hook for failure detection: make rank `rank`'s push skip its rows in

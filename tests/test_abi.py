@@ -55,8 +55,8 @@ def test_host_checks_without_device(lib):
     assert lib.hg_parity(None) == -1
     assert lib.hg_destroy(None) == hg.HG_OK
     assert lib.hg_debug_skip_push(None, 0) == hg.HG_ERR_ARG
-    c, t = ctypes.c_int(), ctypes.c_int()
-    assert lib.hg_launch_shape(None, 1, ctypes.byref(c), ctypes.byref(t)) == hg.HG_ERR_ARG
+    c = ctypes.c_int()
+    assert lib.hg_launch_shape(None, 1, ctypes.byref(c), None, None, None) == hg.HG_ERR_ARG
     assert lib.hg_stock_gather(0, 8, None, None, 1, None) == hg.HG_ERR_ARG
     for code in range(7):
         assert lib.hg_strerror(code)

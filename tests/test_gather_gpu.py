@@ -96,11 +96,21 @@ def test_parity_vs_oracle(tp, W, cap, Ms):
     run_sequence(tp, W, cap, Ms)
 
 
-@pytest.mark.parametrize("threads,ctas", [(128, 1), (128, 3), (256, 7), (512, 2), (128, 0)])
-def test_launch_shapes_vs_oracle(threads, ctas):
-    """Forced small grids make every CTA loop over many units (and a single CTA
-    consume its own pushes one iteration later)."""
-    run_sequence(4, 2048, 6, [6, 1, 5, 6], threads=threads, ctas=ctas)
+@pytest.mark.parametrize("vpt,ctas,mode,coop", [
+    (1, 1, 0, False), (1, 3, 2, False), (2, 7, 0, False), (4, 2, 1, False), (2, 0, 1, False),
+    (4, 0, 2, False), (1, 0, 0, True), (4, 5, 2, True), (0, 0, 0, True)])
+def test_launch_shapes_vs_oracle(vpt, ctas, mode, coop):
+    """Forced launch shapes: small grids make every CTA loop over many units (a
+    single CTA consumes its own pushes one iteration later); pipelined and
+    simple polls; cooperative and programmatic-dependent launches."""
+    run_sequence(4, 2048, 6, [6, 1, 5, 6], elems_per_lane=vpt, ctas=ctas, poll_mode=mode,
+                 cooperative=coop)
+
+
+@pytest.mark.parametrize("tp", [24, 32])
+def test_wide_tp_vs_oracle(tp):
+    """TP above 16 runs 1024-thread CTAs (one warp per rank)."""
+    run_sequence(tp, 256, 3, [3, 1, 2])
 
 
 def test_config2_decode_m1():

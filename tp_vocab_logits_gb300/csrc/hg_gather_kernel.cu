@@ -8,34 +8,51 @@
 // each rank polls its mailbox row until no sentinel word is left, copies it to
 // its [M, V] output and writes the sentinel back.
 //
-// Work decomposition. A unit is (row m, source rank r, chunk c): blockDim.x
-// consecutive elements (16-byte vectors, or 32-bit words when W % 8 != 0) of
-// rank r's row m, one per thread. Units are dealt round-robin to the CTAs;
-// in iteration t CTA g pushes unit t*G + g into all TP mailboxes and consumes,
-// for every consumer rank d, the unit that CTA g+1 (mod G) pushed in iteration
-// t-1. Every poll therefore waits on words that another CTA stores, and a
-// CTA's push never depends on a poll, so with all CTAs co-resident (the
-// launch is cooperative) every wait ends; each one is also bounded in time by
-// %globaltimer and gives up with an error in the status word instead of
-// spinning on. The one-iteration lag keeps the freshly pushed unit in L2
-// until it is polled and decouples neighbouring CTAs.
+// Work decomposition. A CTA has one warp per virtual rank d (blockDim.x = 32 *
+// tp); warp d owns rank d's mailbox and output. A unit is (row m, source rank
+// r, chunk c): 32 * VPT consecutive elements (16-byte vectors, or 32-bit words
+// when W % 8 != 0) of rank r's row m, VPT per lane. Units are dealt
+// round-robin to the CTAs. In iteration t, CTA g pushes unit t*G + g (warp d
+// reads the shard elements, through L1, and stores them into mailbox d) and
+// consumes the unit that CTA g+1 (mod G) pushed in iteration t-1 (warp d polls
+// mailbox d, then writes out[d] and re-arms). Every poll therefore waits on
+// words that another CTA stores, and a push never depends on a poll, so with
+// all CTAs resident every wait ends. The host never launches more CTAs than
+// can be co-resident; each wait is also bounded in time by %globaltimer and
+// gives up with an error in the status word instead of spinning on. The
+// one-iteration lag keeps a pushed unit in L2 until it is polled and decouples
+// neighbouring CTAs.
 //
-// Memory ordering. Pushes and polls are relaxed at gpu scope (morally strong,
-// per-word single-copy atomic; a vector access is one access per 32-bit word),
-// so a polled word is either still the sentinel or the pushed data word, never
-// a mix. A word is re-armed by the thread that read it, after reading it
-// (same-address coherence). Calls are ordered by kernel boundaries on one
-// stream; two calls in a row use different mailbox parities.
+// Polling. PIPE (single-wave launches, where the poll races the neighbour's
+// push): two staggered loads per waiting element stay in flight, so a word
+// that lands between two polls is seen about half an L2 round trip later
+// rather than a whole one. Otherwise (multi-iteration launches, where the data
+// was pushed an iteration earlier): load, check, re-load what is missing.
+//
+// Memory ordering. Pushes, polls and re-arms are relaxed at gpu scope (morally
+// strong, per-word single-copy atomic; a vector access is one access per
+// 32-bit word), so a polled word is either still the sentinel or the pushed
+// data word, never a mix. A word is re-armed by the thread that read it, after
+// reading it (same-address coherence). Calls are ordered by kernel boundaries
+// (a programmatic dependent launch waits for the previous kernel's completion
+// before any access); two calls in a row use different mailbox parities.
 
 #include "hg_internal.cuh"
 
 namespace hg {
 namespace {
 
+constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kPollStaggerNs = 256;  // delay between the two in-flight polls
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ void sleep_ns(unsigned ns) {
+  asm volatile("nanosleep.u32 %0;" :: "r"(ns));
 }
 
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
@@ -52,7 +69,7 @@ template <>
 struct Elem<uint4> {
   static __device__ __forceinline__ uint4 ld_shard(const uint4* p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
   }
@@ -62,13 +79,18 @@ struct Elem<uint4> {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
     return v;
   }
-  static __device__ __forceinline__ void st_push(uint4* p, uint4 v) {
+  static __device__ __forceinline__ void st_relaxed(uint4* p, uint4 v) {
     asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
   }
+  template <bool STREAM>
   static __device__ __forceinline__ void st_out(uint4* p, uint4 v) {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
-                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+    if (STREAM)
+      asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                   :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+    else
+      asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                   :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
   }
   static __device__ __forceinline__ bool arrived(uint4 v) {
     return v.x != kSentinel && v.y != kSentinel && v.z != kSentinel && v.w != kSentinel;
@@ -82,7 +104,6 @@ struct Elem<uint4> {
   static __device__ __forceinline__ uint4 sentinel() {
     return make_uint4(kSentinel, kSentinel, kSentinel, kSentinel);
   }
-  static __device__ __forceinline__ uint4 none() { return make_uint4(0, 0, 0, 0); }
 };
 
 // One 32-bit word (shards whose width is not a multiple of 8 columns).
@@ -90,7 +111,7 @@ template <>
 struct Elem<uint32_t> {
   static __device__ __forceinline__ uint32_t ld_shard(const uint32_t* p) {
     uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
   }
   static __device__ __forceinline__ uint32_t ld_poll(const uint32_t* p) {
@@ -98,149 +119,173 @@ struct Elem<uint32_t> {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
   }
-  static __device__ __forceinline__ void st_push(uint32_t* p, uint32_t v) {
+  static __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
   }
+  template <bool STREAM>
   static __device__ __forceinline__ void st_out(uint32_t* p, uint32_t v) {
-    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+    if (STREAM)
+      asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+    else
+      asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
   }
   static __device__ __forceinline__ bool arrived(uint32_t v) { return v != kSentinel; }
   static __device__ __forceinline__ uint32_t rewrite(uint32_t v) {
     return v == kSentinel ? kSentAs : v;
   }
   static __device__ __forceinline__ uint32_t sentinel() { return kSentinel; }
-  static __device__ __forceinline__ uint32_t none() { return 0u; }
 };
 
-// Where unit u's elements live for this thread.
+// Element offsets of unit u for this lane's slot 0 (slot v adds 32 * v).
 struct UnitPos {
   int r;       // source rank
-  size_t src;  // element offset in the shard of rank r
-  size_t dst;  // element offset in a mailbox row block / output
-  bool valid;  // this thread has an element in the unit
+  int idx;     // element index of slot 0 within the rank-row
+  size_t src;  // offset in rank r's shard
+  size_t dst;  // offset in a mailbox parity and in an output
 };
 
-__device__ __forceinline__ UnitPos unit_pos(const GatherArgs& a, int tp, int u) {
-  const int per_row = tp * a.chunks;
+template <int VPT>
+__device__ __forceinline__ UnitPos unit_pos(const GatherArgs& a, int u, int lane) {
+  const int per_row = a.tp * a.chunks;
   const int m = u / per_row;
   const int rem = u - m * per_row;
   const int r = rem / a.chunks;
   const int c = rem - r * a.chunks;
-  const int idx = c * (int)blockDim.x + (int)threadIdx.x;
   UnitPos p;
   p.r = r;
-  p.valid = idx < a.wv;
-  p.src = (size_t)m * a.wv + idx;
-  p.dst = (size_t)m * tp * a.wv + (size_t)r * a.wv + idx;
+  p.idx = c * 32 * VPT + lane;
+  p.src = (size_t)m * a.wv + p.idx;
+  p.dst = (size_t)m * a.tp * a.wv + (size_t)r * a.wv + p.idx;
   return p;
 }
 
-// Poll NB mailbox elements (consumer ranks d0 .. d0+nb-1) already loaded into
-// x until none holds a sentinel word, then copy them to the outputs and
-// re-arm. Warp-uniform loop: the warp spins until every lane's elements have
-// arrived (warp vote), re-reading only what is still missing. Returns false if
-// the poll gave up (timeout or an error raised elsewhere in the grid).
-template <typename V, int NB>
-__device__ __forceinline__ bool finish_consume(const GatherArgs& a, int d0, int nb,
-                                               const UnitPos& p, V (&x)[NB], int u) {
-  using E = Elem<V>;
-  bool ok = true;
-  unsigned long long t_wait = 0;  // start of this wait, read on the first miss
-#pragma unroll
-  for (int i = 0; i < NB; ++i)
-    if (i < nb) ok = ok && E::arrived(x[i]);
-  if (!p.valid) ok = true;
-  bool gave_up = false;
-  while (!__all_sync(0xffffffffu, ok)) {
-    if (!ok) {
-      ok = true;
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        if (i < nb && !E::arrived(x[i])) {
-          x[i] = E::ld_poll(reinterpret_cast<const V*>(a.box[d0 + i]) + p.dst);
-          ok = ok && E::arrived(x[i]);
-        }
-      }
-      if (!ok && t_wait == 0) t_wait = globaltimer_ns();
-      if (!ok && (globaltimer_ns() - t_wait > a.timeout_ns ||
-                  ld_relaxed_s32(a.status) != kDevOk)) {
-        if (atomicCAS(a.status, kDevOk, kDevTimeout) == kDevOk) {
-          a.status[1] = u;
-          a.status[2] = d0;
-          a.status[3] = (int)p.dst;
-        }
-        gave_up = true;
-        ok = true;
-      }
-    }
+// Record where a poll gave up (the first one wins).
+__device__ __forceinline__ void record_timeout(const GatherArgs& a, int u, int d, size_t dst) {
+  if (atomicCAS(a.status, kDevOk, kDevTimeout) == kDevOk) {
+    a.status[1] = u;
+    a.status[2] = d;
+    a.status[3] = (int)dst;
   }
-  // Give up as a warp, so that no lane leaves while the others vote again.
-  gave_up = __any_sync(0xffffffffu, gave_up);
-  if (!p.valid || gave_up) return !gave_up;
-#pragma unroll
-  for (int i = 0; i < NB; ++i) {
-    if (i < nb) {
-      E::st_out(reinterpret_cast<V*>(a.out[d0 + i]) + p.dst, x[i]);
-      E::st_push(reinterpret_cast<V*>(a.box[d0 + i]) + p.dst, E::sentinel());
-    }
-  }
-  return true;
 }
 
-// TPC > 0: tp known at compile time, all TP consumer elements in flight at
-// once. TPC == 0: any tp, consumer ranks in batches of 4.
-template <typename V, int TPC>
-__global__ void __launch_bounds__(512) gather_kernel(const __grid_constant__ GatherArgs a) {
+template <typename V, int VPT>
+__device__ __forceinline__ void issue_polls(const V* box, const UnitPos& p, unsigned todo,
+                                            V (&q)[VPT]) {
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+    if (todo >> v & 1) q[v] = Elem<V>::ld_poll(box + p.dst + 32 * v);
+}
+
+// Take the arrived elements of q into res; true when this warp is done. A lane
+// that waits too long (or sees an error raised elsewhere) gives up.
+template <typename V, int VPT>
+__device__ __forceinline__ bool take_arrived(const GatherArgs& a, const V (&q)[VPT],
+                                             V (&res)[VPT], unsigned& todo,
+                                             unsigned long long& t_wait, bool& gave_up, int u,
+                                             int d, size_t dst) {
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+    if ((todo >> v & 1) && Elem<V>::arrived(q[v])) {
+      res[v] = q[v];
+      todo &= ~(1u << v);
+    }
+  if (todo) {
+    const unsigned long long now = globaltimer_ns();
+    if (t_wait == 0) t_wait = now;
+    if (now - t_wait > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+      record_timeout(a, u, d, dst);
+      gave_up = true;
+      todo = 0;
+    }
+  }
+  return __all_sync(kFull, todo == 0);
+}
+
+// Poll this lane's elements of unit u in mailbox `box` until none holds a
+// sentinel word; res receives the data. The warp leaves together (vote).
+// Returns false when the warp gave up.
+template <typename V, int VPT, bool PIPE>
+__device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, const UnitPos& p,
+                                          int u, int d, V (&res)[VPT]) {
+  unsigned todo = 0;  // bit v: slot v still waits
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+    if (p.idx + 32 * v < a.wv) todo |= 1u << v;
+  unsigned long long t_wait = 0;
+  bool gave_up = false;
+  V q0[VPT], q1[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) q0[v] = q1[v] = Elem<V>::sentinel();
+  issue_polls<V, VPT>(box, p, todo, q0);
+  if (PIPE) {
+    // Two loads in flight, issued a stagger apart; the loop is unrolled by two
+    // so that no register copy waits on a pending load.
+    for (;;) {
+      sleep_ns(kPollStaggerNs);
+      issue_polls<V, VPT>(box, p, todo, q1);
+      if (take_arrived<V, VPT>(a, q0, res, todo, t_wait, gave_up, u, d, p.dst)) break;
+      sleep_ns(kPollStaggerNs);
+      issue_polls<V, VPT>(box, p, todo, q0);
+      if (take_arrived<V, VPT>(a, q1, res, todo, t_wait, gave_up, u, d, p.dst)) break;
+    }
+  } else {
+    while (!take_arrived<V, VPT>(a, q0, res, todo, t_wait, gave_up, u, d, p.dst))
+      issue_polls<V, VPT>(box, p, todo, q0);
+  }
+  return !__any_sync(kFull, gave_up);
+}
+
+// VPT: elements per lane per unit. PIPE: staggered double polls (single-wave
+// launches). STREAM: evict-first stores of the outputs (multi-iteration
+// launches, whose outputs L2 should not keep). MAXT: largest CTA (32 * tp).
+template <typename V, int VPT, bool PIPE, bool STREAM, int MAXT>
+__global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
-  constexpr int NB = TPC > 0 ? TPC : 4;
-  const int tp = TPC > 0 ? TPC : a.tp;
-  const int N = a.M * tp * a.chunks;  // units
+  // Programmatic dependent launch: wait until the previous kernel on the
+  // stream has completed and its memory is visible, then let the next kernel
+  // start launching. Nothing is read or written before the wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const int lane = (int)threadIdx.x & 31;
+  const int d = (int)threadIdx.x >> 5;  // this warp's rank: mailbox and output
+  // One load per warp of one address: every lane sees the same value.
+  if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
+
+  const int N = a.M * a.tp * a.chunks;  // units
   const int G = (int)gridDim.x;
   const int g = (int)blockIdx.x;
   const int cons = (g + 1 == G) ? 0 : g + 1;  // the CTA whose pushes we consume
   const int iters = (N + G - 1) / G;
-
-  // One load per warp of one address: every lane sees the same value.
-  const int status0 = ld_relaxed_s32(a.status);
+  V* const box = reinterpret_cast<V*>(a.box[d]);
+  V* const out = reinterpret_cast<V*>(a.out[d]);
 
   for (int t = 0; t <= iters; ++t) {
-    // Loads first (push source of iteration t, poll of iteration t-1), so that
-    // their latencies overlap; then the push stores; then the poll.
     const int up = t * G + g;
-    const bool do_push = t < iters && up < N;
-    UnitPos pp{};
-    V xs = E::none();
-    if (do_push) {
-      pp = unit_pos(a, tp, up);
-      if (pp.valid && pp.r != a.skip_rank)
-        xs = E::ld_shard(reinterpret_cast<const V*>(a.shard[pp.r]) + pp.src);
+    if (t < iters && up < N) {
+      const UnitPos p = unit_pos<VPT>(a, up, lane);
+      if (p.r != a.skip_rank) {
+        const V* src = reinterpret_cast<const V*>(a.shard[p.r]) + p.src;
+        V x[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+          if (p.idx + 32 * v < a.wv) x[v] = E::ld_shard(src + 32 * v);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+          if (p.idx + 32 * v < a.wv) E::st_relaxed(box + p.dst + 32 * v, E::rewrite(x[v]));
+      }
     }
     const int uc = (t - 1) * G + cons;
-    const bool do_cons = t >= 1 && uc < N;
-    UnitPos pc{};
-    V x[NB];
-    if (do_cons) {
-      pc = unit_pos(a, tp, uc);
+    if (t >= 1 && uc < N) {
+      const UnitPos p = unit_pos<VPT>(a, uc, lane);
+      V res[VPT];
+      if (!poll_unit<V, VPT, PIPE>(a, box, p, uc, d, res)) return;
 #pragma unroll
-      for (int i = 0; i < NB; ++i)
-        x[i] = (pc.valid && i < tp) ? E::ld_poll(reinterpret_cast<const V*>(a.box[i]) + pc.dst)
-                                    : E::none();
-    }
-    if (status0 != kDevOk) return;  // handle in error state: no device work
-    if (do_push && pp.valid && pp.r != a.skip_rank) {
-      const V y = E::rewrite(xs);
-      for (int d = 0; d < tp; ++d) E::st_push(reinterpret_cast<V*>(a.box[d]) + pp.dst, y);
-    }
-    if (do_cons) {
-      if (!finish_consume<V, NB>(a, 0, tp < NB ? tp : NB, pc, x, uc)) return;
-      for (int d0 = NB; d0 < tp; d0 += NB) {  // only when TPC == 0 and tp > 4
-        const int nb = tp - d0 < NB ? tp - d0 : NB;
-#pragma unroll
-        for (int i = 0; i < NB; ++i)
-          x[i] = (pc.valid && i < nb)
-                     ? E::ld_poll(reinterpret_cast<const V*>(a.box[d0 + i]) + pc.dst)
-                     : E::none();
-        if (!finish_consume<V, NB>(a, d0, nb, pc, x, uc)) return;
+      for (int v = 0; v < VPT; ++v) {
+        if (p.idx + 32 * v < a.wv) {
+          E::template st_out<STREAM>(out + p.dst + 32 * v, res[v]);
+          E::st_relaxed(box + p.dst + 32 * v, E::sentinel());
+        }
       }
     }
   }
@@ -252,42 +297,59 @@ __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
     p[i] = v;
 }
 
-template <typename V>
-const void* pick_kernel(int tp) {
-  switch (tp) {
-    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2>);
-    case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4>);
-    case 8: return reinterpret_cast<const void*>(&gather_kernel<V, 8>);
-    case 16: return reinterpret_cast<const void*>(&gather_kernel<V, 16>);
-    default: return reinterpret_cast<const void*>(&gather_kernel<V, 0>);
+// Kernels for tp <= 16 (CTAs of up to 512 threads) take 1, 2 or 4 elements
+// per lane; larger tp (up to 1024 threads, 64 registers) 1 or 2.
+template <typename V, bool PIPE>
+const void* pick_vpt(int vpt, int tp) {
+  if (tp <= 16) {
+    switch (vpt) {
+      case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 512>);
+      case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 512>);
+      case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4, PIPE, !PIPE, 512>);
+      default: return nullptr;
+    }
+  }
+  switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 1024>);
+    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 1024>);
+    default: return nullptr;
   }
 }
 
-const void* kernel_for(bool vec16, int tp) {
-  return vec16 ? pick_kernel<uint4>(tp) : pick_kernel<uint32_t>(tp);
+const void* kernel_for(const LaunchShape& s, bool vec16, int tp) {
+  if (vec16) return s.pipe ? pick_vpt<uint4, true>(s.vpt, tp) : pick_vpt<uint4, false>(s.vpt, tp);
+  return s.pipe ? pick_vpt<uint32_t, true>(s.vpt, tp) : pick_vpt<uint32_t, false>(s.vpt, tp);
 }
 
 }  // namespace
 
-cudaError_t gather_occupancy(bool vec16, int tp, int threads, int* ctas_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, kernel_for(vec16, tp),
-                                                       threads, 0);
+cudaError_t gather_occupancy(const LaunchShape& s, bool vec16, int tp, int* ctas_per_sm) {
+  const void* k = kernel_for(s, vec16, tp);
+  if (!k) return cudaErrorInvalidValue;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, k, 32 * tp, 0);
 }
 
-cudaError_t launch_gather(const GatherArgs& a, bool vec16, int ctas, int threads,
-                          cudaStream_t stream) {
+cudaError_t launch_gather(const GatherArgs& a, const LaunchShape& s, bool vec16,
+                          cudaStream_t stream, bool cooperative) {
+  const void* k = kernel_for(s, vec16, a.tp);
+  if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3((unsigned)threads);
+  cfg.gridDim = dim3((unsigned)s.ctas);
+  cfg.blockDim = dim3((unsigned)(32 * a.tp));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {const_cast<GatherArgs*>(&a)};
-  return cudaLaunchKernelExC(&cfg, kernel_for(vec16, a.tp), args);
+  return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 cudaError_t launch_fill_u32(uint32_t* p, size_t n, uint32_t v, cudaStream_t stream) {

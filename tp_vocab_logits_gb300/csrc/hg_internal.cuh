@@ -32,16 +32,26 @@ struct GatherArgs {
   int tp;
   int wv;         // elements per rank-row
   int M;          // rows of this call
-  int chunks;     // units per rank-row: ceil(wv / blockDim.x)
+  int chunks;     // units per rank-row: ceil(wv / (32 * vpt))
   int skip_rank;  // test hook: rank whose push is skipped (-1: none)
 };
 
-// Largest co-resident CTAs per SM of the gather kernel for this shape.
-cudaError_t gather_occupancy(bool vec16, int tp, int threads, int* ctas_per_sm);
+// Launch shape of one row count: CTAs (32 * tp threads each), elements per lane
+// per unit, and the polling mode (pipelined for single-wave launches).
+struct LaunchShape {
+  int ctas = 0;
+  int vpt = 1;
+  bool pipe = true;
+};
 
-// Cooperative launch of the gather kernel: all `ctas` CTAs co-resident.
-cudaError_t launch_gather(const GatherArgs& a, bool vec16, int ctas, int threads,
-                          cudaStream_t stream);
+// Largest co-resident CTAs per SM of the gather kernel for this shape.
+cudaError_t gather_occupancy(const LaunchShape& s, bool vec16, int tp, int* ctas_per_sm);
+
+// Launch of the gather kernel. cooperative: the runtime guarantees that all
+// CTAs are co-resident (or fails the launch); otherwise a programmatic
+// dependent launch (the kernel waits for its predecessor before any access).
+cudaError_t launch_gather(const GatherArgs& a, const LaunchShape& s, bool vec16,
+                          cudaStream_t stream, bool cooperative);
 
 // Fill n 32-bit words with v.
 cudaError_t launch_fill_u32(uint32_t* p, size_t n, uint32_t v, cudaStream_t stream);

@@ -28,8 +28,8 @@ class HGError(RuntimeError):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("poll_timeout_ns", ctypes.c_uint64), ("threads", ctypes.c_int),
-                ("ctas", ctypes.c_int)]
+    _fields_ = [("poll_timeout_ns", ctypes.c_uint64), ("elems_per_lane", ctypes.c_int),
+                ("ctas", ctypes.c_int), ("poll_mode", ctypes.c_int), ("cooperative", ctypes.c_int)]
 
 
 _LIB: ctypes.CDLL | None = None
@@ -58,7 +58,8 @@ def load() -> ctypes.CDLL:
     lib.hg_rearm.argtypes = [vp, st]
     lib.hg_parity.argtypes = [vp]
     lib.hg_mailbox.argtypes = [vp, i, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)]
-    lib.hg_launch_shape.argtypes = [vp, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    ip = ctypes.POINTER(i)
+    lib.hg_launch_shape.argtypes = [vp, i, ip, ip, ip, ip]
     lib.hg_debug_skip_push.argtypes = [vp, i]
     lib.hg_stock_gather.argtypes = [i, i, vpp, vpp, i, st]
     lib.hg_strerror.argtypes = [i]
@@ -118,13 +119,14 @@ class Handle:
 
 
 def hg_create(tp: int, shard_cols: int, cap: int, rows: Sequence[int] | None = None, *,
-              poll_timeout_ns: int = 0, threads: int = 0, ctas: int = 0) -> Handle:
+              poll_timeout_ns: int = 0, elems_per_lane: int = 0, ctas: int = 0,
+              poll_mode: int = 0, cooperative: bool = False) -> Handle:
     lib = load()
     rows = list(rows or [])
     arr = (ctypes.c_int * max(1, len(rows)))(*rows)
     out = ctypes.c_void_p()
-    if poll_timeout_ns or threads or ctas:
-        opt = _Options(poll_timeout_ns, threads, ctas)
+    if poll_timeout_ns or elems_per_lane or ctas or poll_mode or cooperative:
+        opt = _Options(poll_timeout_ns, elems_per_lane, ctas, poll_mode, int(bool(cooperative)))
         st = lib.hg_create_ex(tp, shard_cols, cap, arr, len(rows), ctypes.byref(opt),
                               ctypes.byref(out))
     else:
@@ -199,11 +201,11 @@ def hg_mailbox(h: Handle, rank: int) -> tuple:
 
 
 class _DeviceView:
-    """Read-only view of library-owned device memory for torch.as_tensor."""
+    """View of library-owned device memory for torch.as_tensor (only read)."""
 
     def __init__(self, ptr: int, shape: tuple, typestr: str):
         self.__cuda_array_interface__ = {"shape": shape, "typestr": typestr,
-                                         "data": (ptr, True), "version": 3, "strides": None}
+                                         "data": (ptr, False), "version": 3, "strides": None}
 
 
 def mailbox_words(h: Handle, rank: int) -> torch.Tensor:
@@ -216,10 +218,13 @@ def mailbox_words(h: Handle, rank: int) -> torch.Tensor:
     return view.clone()
 
 
-def hg_launch_shape(h: Handle, M: int) -> tuple:
-    c, t = ctypes.c_int(), ctypes.c_int()
-    _check(load().hg_launch_shape(h.ptr, M, ctypes.byref(c), ctypes.byref(t)), "hg_launch_shape")
-    return c.value, t.value
+def hg_launch_shape(h: Handle, M: int) -> dict:
+    """Launch shape of row count M: ctas, threads, elems_per_lane, pipelined."""
+    c, t, e, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load().hg_launch_shape(h.ptr, M, ctypes.byref(c), ctypes.byref(t), ctypes.byref(e),
+                                  ctypes.byref(p)), "hg_launch_shape")
+    return {"ctas": c.value, "threads": t.value, "elems_per_lane": e.value,
+            "pipelined": bool(p.value)}
 
 
 def hg_debug_skip_push(h: Handle, rank: int) -> None:
