@@ -177,6 +177,48 @@ int hg_debug_skip_push(hg_handle *h, int rank);
 int hg_stock_gather(int tp, int shard_cols, const void *const *shard_ptrs,
                     void *const *out_ptrs, int M, hg_stream_t stream);
 
+/* Largest mailbox that one hg_gather_static call may use, in bytes:
+ * tp * M * tp * shard_cols * 2 (every rank's [M, V] BF16 rows, one parity). */
+#define HG_STATIC_MAILBOX_BYTES (24u * 1024u * 1024u)
+
+/*
+ * hg_gather_static - hg_gather for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point: their gather always owns a
+ * mailbox allocated at construction.
+ *
+ * Some callers cannot call cudaMalloc: a serving engine whose caching
+ * allocator has already reserved the GPU's free memory, a plug-in inside a
+ * host framework that forbids allocations outside its own allocator, or a
+ * latency-critical loop that cannot pay for cudaMalloc/cudaFree's implicit
+ * device synchronisation. This call allocates nothing. Its mailbox and status
+ * words live in a fixed __device__ array inside the library
+ * (HG_STATIC_MAILBOX_BYTES + 256 bytes), which every GPU that loads the
+ * library holds until the process exits.
+ *
+ *   tp, shard_cols  as for hg_create (1 <= tp <= HG_MAX_TP, shard_cols even)
+ *   shard_ptrs      tp device pointers to [M, shard_cols] BF16, as for hg_gather
+ *   out_ptrs        tp device pointers to [M, tp * shard_cols] BF16, as for
+ *                   hg_gather
+ *   M               rows, >= 1, with tp * M * tp * shard_cols * 2 <=
+ *                   HG_STATIC_MAILBOX_BYTES
+ *   status_out      optional device pointer to one int32 that receives, in
+ *                   stream order, 0 on success or 1 if a poll gave up; NULL: not
+ *                   reported
+ *   stream          the stream of the call
+ *
+ * Same result as hg_gather on the same shards. The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress, with that device
+ * current), so make that first call before any stream capture. Every call
+ * shares the array and finds it as the previous call left it: each call clears
+ * the status words and re-arms its mailbox region before gathering, on
+ * `stream`. Calls whose device work overlaps (other streams or threads) race on
+ * the array. No parity state is kept. Errors, before any device work:
+ * HG_ERR_ARG (bad sizes, NULL or misaligned pointers, or a mailbox larger than
+ * HG_STATIC_MAILBOX_BYTES), HG_ERR_CUDA (device lookup or launch failed).
+ */
+int hg_gather_static(int tp, int shard_cols, const void *const *shard_ptrs,
+                     void *const *out_ptrs, int M, int *status_out, hg_stream_t stream);
+
 /* Human-readable text of a status code; never NULL. */
 const char *hg_strerror(int status);
 

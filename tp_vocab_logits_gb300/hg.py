@@ -240,3 +240,37 @@ def hg_stock_gather(shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor]
     _check_tensors(outs, tp, tp * W, M, "outs")
     _check(load().hg_stock_gather(tp, W, _ptr_array(shards), _ptr_array(outs), M,
                                   _stream_ptr(stream)), "hg_stock_gather")
+
+
+HG_STATIC_MAILBOX_BYTES = 24 * 1024 * 1024
+
+
+def hg_gather_static(shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
+                     M: int | None = None, status_out: torch.Tensor | None = None,
+                     stream=None) -> None:
+    """The gather without any allocation (libhg's hg_gather_static), for callers
+    that cannot allocate device memory; its mailbox is a fixed array inside the
+    library, shared by every call. shards/outs as for hg_gather; status_out, if
+    given, is a one-element int32 device tensor set to 0 (ok) or 1 (a poll gave
+    up) in stream order."""
+    fn = load().hg_gather_static
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_void_p),
+                   ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    tp = len(shards)
+    M = shards[0].shape[0] if M is None else M
+    W = shards[0].shape[1]
+    need = tp * M * tp * W * 2
+    if need > HG_STATIC_MAILBOX_BYTES:
+        raise ValueError(f"hg_gather_static: tp={tp}, M={M}, shard_cols={W} needs {need} "
+                         f"bytes of mailbox, the fixed maximum is {HG_STATIC_MAILBOX_BYTES}")
+    _check_tensors(shards, tp, W, M, "shards")
+    _check_tensors(outs, tp, tp * W, M, "outs")
+    st_ptr = None
+    if status_out is not None:
+        if not status_out.is_cuda or status_out.dtype != torch.int32 or status_out.numel() < 1:
+            raise ValueError("status_out: need an int32 CUDA tensor with one element")
+        st_ptr = status_out.data_ptr()
+    _check(fn(tp, W, _ptr_array(shards), _ptr_array(outs), M, st_ptr, _stream_ptr(stream)),
+           "hg_gather_static")
