@@ -167,6 +167,35 @@ int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *ele
 int hg_debug_skip_push(hg_handle *h, int rank);
 
 /*
+ * hg_gather_fused - the vocab-parallel LM head and the gather in one kernel
+ * (API page, module docstring: the lm_head's [M, V / TP] logits per rank, then
+ * the gather). For every rank r:
+ *   logits_r[m][n] = bf16_rn(sum_k hidden_r[m][k] * weight_r[n][k])
+ * with fp32 accumulation on the tensor cores; the GEMM's epilogue pushes the
+ * bf16 words straight into every rank's mailbox (sentinel rewrite included),
+ * and the same launch polls, copies to out_ptrs and re-arms, exactly as
+ * hg_gather does on those logits. Asynchronous on `stream`; uses parity
+ * hg_parity(h), then flips it.
+ *
+ *   hidden_ptrs  tp device pointers to [M, K] bf16, row-major, 16-byte aligned
+ *   weight_ptrs  tp device pointers to [W, K] bf16 (nn.Linear layout: vocab
+ *                rows, hidden columns), row-major, 16-byte aligned
+ *   logits_ptrs  NULL, or tp device pointers (each may be NULL) that receive
+ *                rank r's bf16 logits [M, W] as computed (before the rewrite)
+ *   out_ptrs     tp device pointers to [M, tp * W] bf16, as for hg_gather
+ *   M            rows: served by the handle and <= 16
+ *   K            hidden size: a positive multiple of 64
+ *
+ * Requires tp <= 16 and W a multiple of 128. Errors, before any device work
+ * and with no parity flip: HG_ERR_ARG, HG_ERR_ROWS, HG_ERR_CAPTURE,
+ * HG_ERR_STATE, HG_ERR_CUDA (launch or tensor-map encoding failed). A wait
+ * that times out is reported by hg_sync, as for hg_gather.
+ */
+int hg_gather_fused(hg_handle *h, const void *const *hidden_ptrs, const void *const *weight_ptrs,
+                    void *const *logits_ptrs, void *const *out_ptrs, int M, int K,
+                    hg_stream_t stream);
+
+/*
  * hg_stock_gather - the baseline without a mailbox: the rank-order concat of
  * NCCL's all-gather (the page's stock LogitsProcessor gather: all-gather into
  * [TP, M, V / TP], then a copy to [M, V]) done as tp * tp cudaMemcpy2DAsync

@@ -1,0 +1,538 @@
+// Fused LM-head producer: the vocab-parallel lm_head GEMM whose epilogue
+// pushes its bf16 logits straight into every rank's Lamport mailbox, followed,
+// in the same persistent kernel, by the poll / copy / re-arm of the gather.
+//
+// What it computes (vLLM API page "vllm.models.kimi_k3.nvidia.
+// specialized_decode.runtime.logits_gather", module docstring: the
+// vocab-parallel lm_head yields [M, V / TP] per rank, then the gather): for
+// every virtual rank r,
+//   logits_r[m][n] = bf16_rn( sum_k hidden_r[m][k] * weight_r[n][k] )
+// with fp32 accumulation (weight_r in the nn.Linear layout [W, K]), and then
+// exactly the gather of hg_gather on those logits: the sentinel word (+0, -0)
+// is sent as (+0, +0) into row m, word column r * W / 2 of every rank's
+// mailbox, and each rank polls, copies its row to the [M, V] output and
+// re-arms.
+//
+// GEMM (tcgen05, swap-AB). The vocab is the MMA's M dimension (128 weight rows
+// per tile) and the M <= 16 hidden rows, zero-padded, are its N = 16. Per
+// 64-wide K block, TMA loads a [128 x 64] weight tile (16 KB) and the [16 x
+// 64] hidden tile (2 KB) into one of kStages shared-memory stages with 128-byte
+// swizzle (the canonical K-major layout of the shared-memory descriptors); one
+// elected thread issues four 128x16x16 bf16 MMAs into an fp32 accumulator in
+// tensor memory (two accumulators of 16 columns, so that the epilogue of one
+// tile overlaps the MMAs of the next). Warp 0 is the TMA producer, warp 1 the
+// MMA issuer (and owner of the TMEM allocation), warps 2..5 the epilogue: each
+// reads its 32 TMEM lanes (= 32 vocab rows) with tcgen05.ld, rounds to bf16,
+// packs column pairs into 32-bit words, rewrites the sentinel and stores the
+// word into all TP mailboxes. The GEMM streams each weight byte from HBM once
+// (evict-first), so the kernel is bound by HBM bandwidth on the weights.
+//
+// Gather. Tiles are dealt round-robin to the CTAs (one CTA per SM, all
+// co-resident: cooperative launch). After its own tiles, CTA g polls the
+// tiles of CTA g+1 (mod G) in every rank's mailbox, copies them to the
+// outputs and re-arms, as the gather kernel does. Every wait in this kernel
+// (mbarriers and polls) is bounded by %globaltimer; on expiry the kernel
+// records the error in the status block, lets its in-flight copies and MMAs
+// drain, frees its tensor memory and returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "hg_internal.cuh"
+
+namespace hg {
+namespace fused {
+namespace {
+
+constexpr int kTileN = 128;      // weight rows (vocab columns) per tile: MMA M
+constexpr int kBlockK = 64;      // K per stage: one 128-byte swizzle atom of bf16
+constexpr int kMmaN = 16;        // padded hidden rows: MMA N
+constexpr int kMmaK = 16;        // K per tcgen05.mma of kind::f16
+constexpr int kStages = 8;
+constexpr uint32_t kABytes = kTileN * kBlockK * 2;  // 16384
+constexpr uint32_t kBBytes = kMmaN * kBlockK * 2;   // 2048
+constexpr int kAccCols = 16;     // fp32 columns of one accumulator
+constexpr uint32_t kTmemCols = 32;  // two accumulators (power of two >= 32)
+constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr size_t kSmemBytes = (size_t)kStages * (kABytes + kBBytes) + 1024 /*align*/ + 256;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), A and B K-major (bits 15,
+// 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// whose 8-row groups are 1024 bytes apart: start address >> 4 (bits 0-13),
+// leading byte offset 16 >> 4 (bits 16-29, unused by this layout), stride
+// byte offset 1024 >> 4 (bits 32-45), descriptor version 1 (bits 46-47),
+// swizzle mode 128B = 2 (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16_f32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kInstrDesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t w;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+  return w;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_poll_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_v4(uint4* p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ bool arrived_v4(uint4 v) {
+  return v.x != kSentinel && v.y != kSentinel && v.z != kSentinel && v.w != kSentinel;
+}
+
+struct Shared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t failed;
+};
+
+__device__ __forceinline__ void raise_error(const FusedArgs& a, int where) {
+  if (atomicCAS(a.status, kDevOk, kDevTimeout) == kDevOk) {
+    a.status[1] = -1;
+    a.status[2] = where;
+    a.status[3] = (int)blockIdx.x;
+  }
+}
+
+// Bounded wait on an mbarrier phase. False: time limit or an error raised
+// elsewhere (recorded in the status block).
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FusedArgs& a, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+      raise_error(a, where);
+      return false;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ FusedArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned operand stages (the 128-byte swizzle repeats every 1024).
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* sA = base;
+  unsigned char* sB = base + (size_t)kStages * kABytes;
+  Shared* sh = reinterpret_cast<Shared*>(sB + (size_t)kStages * kBBytes);
+
+  const int warp = (int)threadIdx.x >> 5;
+  const int lane = (int)threadIdx.x & 31;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh->acc_full[b], 1);
+      mbar_init(&sh->acc_empty[b], 4);  // one arrive per epilogue warp
+    }
+    mbar_init(&sh->drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  const int items = a.tp * a.tiles_per_rank;
+  const int G = (int)gridDim.x;
+  const int g = (int)blockIdx.x;
+  const int kblocks = a.K / kBlockK;
+
+  if (warp == 0) {
+    // TMA producer.
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = g; it < items && ok; it += G) {
+        const int r = it / a.tiles_per_rank;
+        const int t = it - r * a.tiles_per_rank;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&sh->empty[stage], phase ^ 1u, a, 1)) { ok = false; break; }
+          mbar_expect_tx(&sh->full[stage], kABytes + kBBytes);
+          tma_load_2d(sA + (size_t)stage * kABytes, &a.tm_w[r], kb * kBlockK, t * kTileN,
+                      &sh->full[stage], pol_w);
+          tma_load_2d(sB + (size_t)stage * kBBytes, &a.tm_h[r], kb * kBlockK, 0,
+                      &sh->full[stage], pol_h);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // MMA issuer.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int it = g; it < items && ok; it += G) {
+        if (!mbar_wait(&sh->acc_empty[acc], acc_phase ^ 1u, a, 2)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&sh->full[stage], phase, a, 3)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + (size_t)stage * kABytes));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + (size_t)stage * kBBytes));
+#pragma unroll
+          for (int k = 0; k < kBlockK / kMmaK; ++k) {
+            // K step of 16 bf16 = 32 bytes = 2 in the start-address field.
+            mma_bf16_f32(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
+                         (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&sh->empty[stage]);  // stage free once these MMAs have read it
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&sh->acc_full[acc]);  // accumulator ready
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      // Let every MMA this thread issued finish before TMEM is freed.
+      mma_commit(&sh->drain);
+      mbar_wait(&sh->drain, 0, a, 4);
+    }
+  } else {
+    // Epilogue: warps 2..5; warp w reads TMEM lanes 32 * (w % 4) ...
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // vocab row within the tile
+    const int V = a.tp * a.W;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int it = g; it < items; it += G) {
+      // Every lane waits; the vote reconverges the warp before the warp-wide
+      // tcgen05.ld and makes the give-up decision the same for all lanes.
+      const bool ready = mbar_wait(&sh->acc_full[acc], acc_phase, a, 5);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kAccCols), v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+
+      const int r = it / a.tiles_per_rank;
+      const int t = it - r * a.tiles_per_rank;
+      // Word of vocab columns (row, row + 1) of rank r, for even rows.
+      const size_t wcol = (size_t)t * (kTileN / 2) + (size_t)(row >> 1);
+      uint32_t* lg = reinterpret_cast<uint32_t*>(a.logits[r]);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        if (m < a.M) {
+          const float mine = __uint_as_float(v[m]);
+          const float next = __shfl_down_sync(0xffffffffu, mine, 1);
+          if ((lane & 1) == 0) {
+            const uint32_t word = pack_bf16x2(mine, next);  // low half = even column
+            if (lg) lg[(size_t)m * (a.W / 2) + wcol] = word;
+            const uint32_t y = word == kSentinel ? kSentAs : word;
+            const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + wcol;
+            for (int d = 0; d < a.tp; ++d)
+              st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + off, y);
+          }
+        }
+      }
+    }
+  }
+
+  // All roles done (or stopped on an error): free the tensor memory. One
+  // thread reads the status so that every thread takes the same branch.
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) sh->failed = ld_relaxed_s32(a.status) != kDevOk ? 1u : 0u;
+  __syncthreads();
+  tc_fence_after();
+  const bool failed = sh->failed != 0;
+  if (failed) {
+    // Let in-flight TMA copies and MMAs land before the CTA's memory goes.
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();  // the warp-wide dealloc needs the whole warp converged
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+  if (failed) return;
+
+  // Gather: poll the tiles of CTA g+1 in every rank's mailbox, copy, re-arm.
+  const int cons = (g + 1 == G) ? 0 : g + 1;
+  const int V = a.tp * a.W;
+  const int per_item = a.tp * a.M * (kTileN / 8);  // 16-byte vectors per tile
+  const uint4 sent = make_uint4(kSentinel, kSentinel, kSentinel, kSentinel);
+  for (int it = cons; it < items; it += G) {
+    const int r = it / a.tiles_per_rank;
+    const int t = it - r * a.tiles_per_rank;
+    for (int j = (int)threadIdx.x; j < per_item; j += kThreads) {
+      const int d = j / (a.M * (kTileN / 8));
+      const int rem = j - d * (a.M * (kTileN / 8));
+      const int m = rem / (kTileN / 8);
+      const int vv = rem - m * (kTileN / 8);
+      const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + (size_t)t * (kTileN / 2) +
+                         (size_t)vv * 4;  // in words
+      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.box[d]) + off);
+      uint4 x = ld_poll_v4(p);
+      if (!arrived_v4(x)) {
+        const unsigned long long t0 = globaltimer_ns();
+        do {
+          x = ld_poll_v4(p);
+          if (arrived_v4(x)) break;
+          if (globaltimer_ns() - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+            raise_error(a, 6);
+            return;
+          }
+        } while (true);
+      }
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.out[d]) + off) = x;
+      st_relaxed_v4(p, sent);
+    }
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map of a row-major [rows, K] matrix, box [box_rows, 64],
+// 128-byte swizzle; rows beyond `rows` read as zero.
+bool encode(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+  EncodeTiled fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {K, rows};
+  cuuint64_t strides[1] = {K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBlockK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int fused_limits(int* max_tp, int* max_m, int* k_multiple, int* w_multiple) {
+  *max_tp = kFusedMaxTp;
+  *max_m = kMmaN;
+  *k_multiple = kBlockK;
+  *w_multiple = kTileN;
+  return 0;
+}
+
+cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
+  FusedArgs a;  // copied into the launch by cudaLaunchKernelExC
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  for (int r = 0; r < l.tp; ++r) {
+    if (!encode(&a.tm_w[r], l.weight[r], (uint64_t)l.W, (uint64_t)l.K, kTileN) ||
+        !encode(&a.tm_h[r], l.hidden[r], (uint64_t)l.M, (uint64_t)l.K, kMmaN))
+      return cudaErrorInvalidValue;
+    a.box[r] = l.box[r];
+    a.out[r] = l.out[r];
+    a.logits[r] = l.logits ? l.logits[r] : nullptr;
+  }
+  for (int r = l.tp; r < kFusedMaxTp; ++r) {
+    a.box[r] = nullptr;
+    a.out[r] = nullptr;
+    a.logits[r] = nullptr;
+  }
+  a.status = l.status;
+  a.timeout_ns = l.timeout_ns;
+  a.tp = l.tp;
+  a.W = l.W;
+  a.K = l.K;
+  a.M = l.M;
+  a.tiles_per_rank = l.W / kTileN;
+  const int items = l.tp * a.tiles_per_rank;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel, kThreads,
+                                                                kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  int grid = sms * per_sm;
+  if (grid > items) grid = items;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&fused_kernel), args);
+}
+
+}  // namespace fused
+}  // namespace hg

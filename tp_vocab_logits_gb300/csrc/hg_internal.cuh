@@ -1,6 +1,7 @@
 // Internal declarations shared by the gather library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -55,5 +56,44 @@ cudaError_t launch_gather(const GatherArgs& a, const LaunchShape& s, bool vec16,
 
 // Fill n 32-bit words with v.
 cudaError_t launch_fill_u32(uint32_t* p, size_t n, uint32_t v, cudaStream_t stream);
+
+namespace fused {
+
+// Largest TP of the fused producer (its kernel argument block holds two tensor
+// maps per rank).
+constexpr int kFusedMaxTp = 16;
+
+// Kernel arguments of the fused LM-head producer + gather.
+struct FusedArgs {
+  CUtensorMap tm_w[kFusedMaxTp];  // rank r's weight [W, K] bf16, box [128, 64]
+  CUtensorMap tm_h[kFusedMaxTp];  // rank r's hidden [M, K] bf16, box [16, 64]
+  void* box[kFusedMaxTp];         // rank d's mailbox, parity in use: [cap][V] bf16
+  void* out[kFusedMaxTp];         // rank d's output [M][V] bf16
+  void* logits[kFusedMaxTp];      // optional: rank r's bf16 logits [M][W] (nullptr: none)
+  int* status;                    // device status words
+  unsigned long long timeout_ns;
+  int tp, W, K, M;
+  int tiles_per_rank;             // W / 128
+};
+
+// Host-side description of one fused call.
+struct FusedLaunch {
+  const void* const* hidden;  // tp device pointers, [M, K] bf16
+  const void* const* weight;  // tp device pointers, [W, K] bf16
+  void* const* logits;        // nullptr, or tp device pointers (entries may be nullptr)
+  void* box[HG_MAX_TP];
+  void* const* out;
+  int* status;
+  unsigned long long timeout_ns;
+  int tp, W, K, M;
+};
+
+// Limits of the fused path: TP, rows, K granularity, W granularity.
+int fused_limits(int* max_tp, int* max_m, int* k_multiple, int* w_multiple);
+
+// Cooperative launch of the fused kernel (one CTA per SM at most).
+cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms);
+
+}  // namespace fused
 
 }  // namespace hg

@@ -293,6 +293,45 @@ int hg_debug_skip_push(hg_handle* h, int rank) {
   return HG_OK;
 }
 
+int hg_gather_fused(hg_handle* h, const void* const* hidden_ptrs, const void* const* weight_ptrs,
+                    void* const* logits_ptrs, void* const* out_ptrs, int M, int K,
+                    hg_stream_t stream) {
+  if (!h || !hidden_ptrs || !weight_ptrs || !out_ptrs) return HG_ERR_ARG;
+  int max_tp = 0, max_m = 0, k_mult = 0, w_mult = 0;
+  hg::fused::fused_limits(&max_tp, &max_m, &k_mult, &w_mult);
+  if (h->tp > max_tp || !h->vec16 || h->W % w_mult != 0 || K < k_mult || K % k_mult != 0)
+    return HG_ERR_ARG;
+  if (M < 1 || M > h->cap || !h->served[M]) return HG_ERR_ROWS;
+  if (M > max_m) return HG_ERR_ARG;
+  if (h->failed) return HG_ERR_STATE;
+  for (int r = 0; r < h->tp; ++r) {
+    if (!hidden_ptrs[r] || !weight_ptrs[r] || !out_ptrs[r] || !aligned(hidden_ptrs[r], 16) ||
+        !aligned(weight_ptrs[r], 16) || !aligned(out_ptrs[r], 16))
+      return HG_ERR_ARG;
+    if (logits_ptrs && logits_ptrs[r] && !aligned(logits_ptrs[r], 4)) return HG_ERR_ARG;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return HG_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return HG_ERR_CAPTURE;
+
+  hg::fused::FusedLaunch l;
+  l.hidden = hidden_ptrs;
+  l.weight = weight_ptrs;
+  l.logits = logits_ptrs;
+  l.out = out_ptrs;
+  for (int d = 0; d < h->tp; ++d)
+    l.box[d] = static_cast<char*>(h->box[d]) + (size_t)h->parity * h->parity_elems * 16;
+  l.status = h->status;
+  l.timeout_ns = h->timeout_ns;
+  l.tp = h->tp;
+  l.W = h->W;
+  l.K = K;
+  l.M = M;
+  if (hg::fused::fused_launch(l, stream, h->sms) != cudaSuccess) return HG_ERR_CUDA;
+  h->parity ^= 1;
+  return HG_OK;
+}
+
 int hg_stock_gather(int tp, int shard_cols, const void* const* shard_ptrs, void* const* out_ptrs,
                     int M, hg_stream_t stream) {
   if (tp < 1 || tp > HG_MAX_TP || shard_cols < 1 || M < 0 || !shard_ptrs || !out_ptrs)

@@ -62,11 +62,12 @@ def load() -> ctypes.CDLL:
     lib.hg_launch_shape.argtypes = [vp, i, ip, ip, ip, ip]
     lib.hg_debug_skip_push.argtypes = [vp, i]
     lib.hg_stock_gather.argtypes = [i, i, vpp, vpp, i, st]
+    lib.hg_gather_fused.argtypes = [vp, vpp, vpp, vpp, vpp, i, i, st]
     lib.hg_strerror.argtypes = [i]
     lib.hg_strerror.restype = ctypes.c_char_p
     for name in ("hg_create", "hg_create_ex", "hg_destroy", "hg_gather", "hg_sync", "hg_rearm",
                  "hg_parity", "hg_mailbox", "hg_launch_shape", "hg_debug_skip_push",
-                 "hg_stock_gather"):
+                 "hg_stock_gather", "hg_gather_fused"):
         getattr(lib, name).restype = i
     _LIB = lib
     return lib
@@ -178,6 +179,27 @@ def hg_gather(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Te
     [M, V] bf16 output (both lists of device tensors)."""
     M = shards[0].shape[0] if M is None else M
     GatherCall(h, shards, outs, M, stream)()
+
+
+def hg_gather_fused(h: Handle, hidden: Sequence[torch.Tensor], weight: Sequence[torch.Tensor],
+                    outs: Sequence[torch.Tensor], M: int | None = None,
+                    logits: Sequence[torch.Tensor] | None = None, stream=None) -> None:
+    """LM head + gather in one launch: hidden[r] is rank r's [M, K] bf16 input,
+    weight[r] its [W, K] bf16 lm_head weight (nn.Linear layout), outs[d] rank
+    d's [M, V] output; logits, if given, receives each rank's [M, W] bf16
+    logits."""
+    M = hidden[0].shape[0] if M is None else M
+    K = hidden[0].shape[1]
+    _check_tensors(hidden, h.tp, K, M, "hidden")
+    _check_tensors(weight, h.tp, K, h.shard_cols, "weight")
+    _check_tensors(outs, h.tp, h.V, M, "outs")
+    lp = None
+    if logits is not None:
+        _check_tensors(logits, h.tp, h.shard_cols, M, "logits")
+        lp = _ptr_array(logits)
+    st = load().hg_gather_fused(h.ptr, _ptr_array(hidden), _ptr_array(weight), lp,
+                                _ptr_array(outs), M, K, _stream_ptr(stream))
+    _check(st, "hg_gather_fused")
 
 
 def hg_sync(h: Handle, stream=None) -> None:
