@@ -410,6 +410,11 @@ def run_ours(args):
         hm.close()
         del sm_, om_, cm_
 
+    # ---- fused LM-head producer (config 5) ----
+    fused = None
+    if not args.quick:
+        fused = run_fused_points(torch, hg, synth, device, [1, 4, 8], 20, 3, stream)
+
     # ---- stock cudaMemcpy2D concat baseline on the step workload ----
     stock_us = None
     if not args.quick:
@@ -461,6 +466,7 @@ def run_ours(args):
         "per_m": per_m,
         "large_m": large,
         "stock_memcpy2d_us_per_call": stock_us,
+        "fused_lm_head": fused,
         "cpu_baseline": cpu,
         "clocks": clocks,
     }
@@ -468,6 +474,65 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+# -------------------------------------------------------------------- fused --
+
+def fused_bytes(tp: int, W: int, K: int, M: int) -> int:
+    """Algorithmic bytes of one fused call: every weight byte once, the hidden
+    rows, and the gather's push, poll, output write and re-arm."""
+    V = tp * W
+    return tp * W * K * 2 + tp * M * K * 2 + 4 * tp * M * V * 2
+
+
+def run_fused_points(torch, hg, synth, device, Ms, reps, warmup, stream, with_unfused=True,
+                     Wd=20480):
+    """Config 5: TP8, V=163840 (W=20480), K=7168; weights resident (2.35 GB,
+    larger than L2). Returns {M: {...}}."""
+    import ctypes
+    tp, K = 8, 7168
+    pk = peaks()
+    weight = [synth.weight(4, r, Wd, K, device=device) for r in range(tp)]
+    res = {}
+    lib = hg.load()
+    for M in Ms:
+        h = hg.hg_create(tp, Wd, max(Ms), rows=sorted(set(Ms)))
+        hid = synth.hidden(4, tp, M, K, device=device)
+        outs = torch.empty((tp, M, tp * Wd), dtype=torch.int16, device=device)
+        hp = (ctypes.c_void_p * tp)(*[hid[r].data_ptr() for r in range(tp)])
+        wp = (ctypes.c_void_p * tp)(*[w.data_ptr() for w in weight])
+        op = (ctypes.c_void_p * tp)(*[outs[d].data_ptr() for d in range(tp)])
+        sp = stream.cuda_stream
+
+        def call():
+            st = lib.hg_gather_fused(h.ptr, hp, wp, None, op, M, K, sp)
+            if st != 0:
+                raise SystemExit(f"hg_gather_fused failed: {hg.strerror(st)}")
+        ms = time_calls(torch, [call], reps, warmup, stream, f"timed_fused_m{M}")
+        hg.hg_sync(h)
+        us = ms * 1000.0 / reps
+        wgbs = tp * Wd * K * 2 / (us * 1e-6) / 1e9
+        entry = {"us_per_call": round(us, 2), "weight_GBps": round(wgbs, 1),
+                 "weight_frac_of_measured_hbm": round(wgbs / pk["hbm_gbs"], 3),
+                 "algorithmic_GBps": round(fused_bytes(tp, Wd, K, M) / (us * 1e-6) / 1e9, 1)}
+        if with_unfused:
+            # Baseline: cuBLAS GEMM per rank (torch.matmul) then the gather.
+            logits = torch.empty((tp, M, Wd), dtype=torch.bfloat16, device=device)
+            hb = hid.view(torch.bfloat16)
+            wb = [w.view(torch.bfloat16) for w in weight]
+            g = hg.GatherCall(h, [logits[r].view(torch.int16) for r in range(tp)],
+                              [outs[d] for d in range(tp)], M)
+
+            def unfused():
+                for r in range(tp):
+                    torch.matmul(hb[r], wb[r].t(), out=logits[r])
+                g()
+            ms2 = time_calls(torch, [unfused], reps, warmup, stream, f"timed_unfused_m{M}")
+            hg.hg_sync(h)
+            entry["unfused_cublas_then_gather_us"] = round(ms2 * 1000.0 / reps, 2)
+        res[str(M)] = entry
+        h.close()
+    return res
 
 
 # -------------------------------------------------------------------- sweep --
@@ -512,6 +577,23 @@ def run_sweep(args):
     return 0
 
 
+def run_fused_only(args):
+    import torch
+
+    from tp_vocab_logits_gb300 import _build, hg, synth
+    _build.build()
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    Ms = [int(x) for x in args.fused_ms.split(",")]
+    res = run_fused_points(torch, hg, synth, device, Ms, args.calls, 3,
+                           torch.cuda.current_stream(), with_unfused=not args.quick,
+                           Wd=args.fused_w)
+    for M, e in res.items():
+        print(json.dumps(dict(e, fused="lm_head+gather", tp=8, shard_cols=args.fused_w, K=7168,
+                              M=int(M))), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,6 +604,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true", help="bandwidth sweep, one line per point")
+    ap.add_argument("--fused", action="store_true",
+                    help="fused LM-head producer only (TP8, K=7168, V=163840), one line per M")
+    ap.add_argument("--fused-ms", default="1,4,8")
+    ap.add_argument("--fused-w", type=int, default=20480, help="fused: shard columns per rank")
     ap.add_argument("--tps", default="2,4,8,16")
     ap.add_argument("--widths", default="4096,8192,20480,65536")
     ap.add_argument("--ms", default="1,8,32,64,128,256")
@@ -538,6 +624,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.fused:
+        return run_fused_only(args)
     return run_ours(args)
 
 
