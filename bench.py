@@ -356,6 +356,33 @@ def run_ours(args):
     ms_max, us_call = replica_us_per_call(dist, ms, args.steps, world, device)
     us_launch = ms * 1000.0 / args.steps  # this rank's average launch duration
 
+    # ---- the same calls captured in a CUDA graph (device-resident parity) ----
+    graph_us = None
+    if not args.quick:
+        hgph, sg, og_, cg = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device,
+                                          device_parity=True)
+        cg[0]()
+        torch.cuda.synchronize()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        n_graph = 200
+        with torch.cuda.stream(gs):
+            calls_g = [hg.GatherCall(hgph, [sg[i % nsets, r] for r in range(TP)],
+                                     [og_[i % nsets, d] for d in range(TP)], M_STEP, stream=gs)
+                       for i in range(n_graph)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for c in calls_g:
+                c()
+        torch.cuda.synchronize()
+        reps = max(1, args.steps // n_graph)
+        gms = time_calls(torch, [graph.replay], reps, 2, stream, "timed_graph")
+        hg.hg_sync(hgph)
+        graph_us = round(gms * 1000.0 / (reps * n_graph), 3)
+        del graph
+        hgph.close()
+        del sg, og_, cg
+
     # ---- e2e: pinned host buffers, H2D + gather + D2H per step ----
     host_in = [torch.empty((TP, M_STEP, W), dtype=torch.int16).pin_memory() for _ in range(3)]
     for s in range(3):
@@ -465,6 +492,7 @@ def run_ours(args):
                              "L2-resident and the launch is latency-bound"},
         "per_m": per_m,
         "large_m": large,
+        "graph_replay_us_per_call": graph_us,
         "stock_memcpy2d_us_per_call": stock_us,
         "fused_lm_head": fused,
         "cpu_baseline": cpu,

@@ -76,6 +76,13 @@ typedef struct hg_options {
                                next call's launch overlaps this one; 1:
                                cooperative launch, the runtime itself checks
                                that every CTA is co-resident (no overlap) */
+  int device_parity;        /* 0 (default): the host keeps the parity and calls
+                               on a capturing stream are refused
+                               (HG_ERR_CAPTURE); 1: the parity lives in device
+                               memory, each call's kernel reads it and flips it
+                               once every CTA has read it, so calls may be
+                               captured into a CUDA graph and replayed; the
+                               host learns the parity only at hg_sync */
 } hg_options;
 
 /*
@@ -124,8 +131,9 @@ int hg_destroy(hg_handle *h);
  * Uses parity hg_parity(h), then flips it. The caller owns the shards and the
  * outputs; the library owns the mailboxes. Errors, all before any device work
  * and with no parity flip: HG_ERR_ARG (NULL handle or pointer, misaligned
- * pointer), HG_ERR_ROWS (M not served), HG_ERR_CAPTURE (stream capturing),
- * HG_ERR_CUDA (launch failed; parity not flipped). A poll that times out on the
+ * pointer), HG_ERR_ROWS (M not served), HG_ERR_CAPTURE (stream capturing,
+ * unless the handle has device_parity), HG_ERR_CUDA (launch failed; parity
+ * not flipped). A poll that times out on the
  * device is reported by the next hg_sync; until hg_rearm every later gather
  * of the handle does no device work.
  */
@@ -143,7 +151,8 @@ int hg_sync(hg_handle *h, hg_stream_t stream);
 int hg_rearm(hg_handle *h, hg_stream_t stream);
 
 /* Parity the next hg_gather uses (0 or 1; starts at 0, flips per served call
- * as `self.parity ^= 1` in HeadGather.__call__), or -1 for NULL. */
+ * as `self.parity ^= 1` in HeadGather.__call__), or -1 for NULL. With
+ * device_parity, the parity as of the last hg_sync or hg_rearm. */
 int hg_parity(const hg_handle *h);
 
 /* Rank `rank`'s mailbox for inspection: device pointer to [2][cap][tp * W]

@@ -255,6 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   const int lane = (int)threadIdx.x & 31;
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  size_t parity_off = 0;  // in 32-bit words
+  if (a.dev_parity) {
+    // Device-resident parity: read by every thread, flipped by the last CTA
+    // to arrive (after every CTA has read it).
+    const int p = ld_relaxed_s32(a.dev_parity);
+    parity_off = (size_t)p * a.parity_stride_words;
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(a.arrivals, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.arrivals, 0);
+      atomicExch(const_cast<int*>(a.dev_parity), p ^ 1);
+    }
+  }
   if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
 
   if (threadIdx.x == 0) {
@@ -378,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
             const uint32_t y = word == kSentinel ? kSentAs : word;
             const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + wcol;
             for (int d = 0; d < a.tp; ++d)
-              st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + off, y);
+              st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off, y);
           }
         }
       }
@@ -422,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       const int vv = rem - m * (kTileN / 8);
       const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + (size_t)t * (kTileN / 2) +
                          (size_t)vv * 4;  // in words
-      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.box[d]) + off);
+      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off);
       uint4 x = ld_poll_v4(p);
       if (!arrived_v4(x)) {
         const unsigned long long t0 = globaltimer_ns();
@@ -507,6 +519,9 @@ cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   }
   a.status = l.status;
   a.timeout_ns = l.timeout_ns;
+  a.dev_parity = l.dev_parity;
+  a.arrivals = l.arrivals;
+  a.parity_stride_words = l.parity_stride_words;
   a.tp = l.tp;
   a.W = l.W;
   a.K = l.K;

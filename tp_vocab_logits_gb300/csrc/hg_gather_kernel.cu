@@ -249,6 +249,18 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
 
   const int lane = (int)threadIdx.x & 31;
   const int d = (int)threadIdx.x >> 5;  // this warp's rank: mailbox and output
+  size_t parity_off = 0;
+  if (a.dev_parity) {
+    // Device-resident parity: every thread reads it, then the last CTA to
+    // arrive flips it for the next call (no CTA can read it after the flip).
+    const int p = ld_relaxed_s32(a.dev_parity);
+    parity_off = (size_t)p * a.parity_stride;
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(a.arrivals, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.arrivals, 0);
+      atomicExch(const_cast<int*>(a.dev_parity), p ^ 1);
+    }
+  }
   // One load per warp of one address: every lane sees the same value.
   if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
 
@@ -257,7 +269,7 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   const int g = (int)blockIdx.x;
   const int cons = (g + 1 == G) ? 0 : g + 1;  // the CTA whose pushes we consume
   const int iters = (N + G - 1) / G;
-  V* const box = reinterpret_cast<V*>(a.box[d]);
+  V* const box = reinterpret_cast<V*>(a.box[d]) + parity_off;
   V* const out = reinterpret_cast<V*>(a.out[d]);
 
   for (int t = 0; t <= iters; ++t) {

@@ -17,10 +17,14 @@ namespace hg {
 constexpr uint32_t kSentinel = 0x80000000u;
 constexpr uint32_t kSentAs = 0x00000000u;
 
-// Device status word values (status[0]); status[1..3] record where a poll
-// gave up: unit index, consumer rank, first word offset.
+// Device status block. status[0]: kDevOk or kDevTimeout; status[1..3]: where
+// a poll gave up (unit index, consumer rank, first word offset);
+// status[kParityWord]: the parity of handles whose parity lives on the device;
+// status[kArrivalsWord]: CTAs of the current call that have read it.
 enum DevStatus : int { kDevOk = 0, kDevTimeout = 1 };
-constexpr int kStatusWords = 4;
+constexpr int kParityWord = 4;
+constexpr int kArrivalsWord = 5;
+constexpr int kStatusWords = 8;
 
 // Arguments of one gather launch. Element = 16-byte vector (vector path) or
 // one 32-bit word (word path).
@@ -35,6 +39,13 @@ struct GatherArgs {
   int M;          // rows of this call
   int chunks;     // units per rank-row: ceil(wv / (32 * vpt))
   int skip_rank;  // test hook: rank whose push is skipped (-1: none)
+  // Device-resident parity: nullptr when box[] already points at the parity in
+  // use; otherwise box[] points at parity 0, parity p adds p * parity_stride
+  // elements, and the kernel reads the parity from here and flips it once
+  // every CTA has read it (arrivals counts them).
+  const int* dev_parity = nullptr;
+  int* arrivals = nullptr;
+  size_t parity_stride = 0;
 };
 
 // Launch shape of one row count: CTAs (32 * tp threads each), elements per lane
@@ -74,6 +85,11 @@ struct FusedArgs {
   unsigned long long timeout_ns;
   int tp, W, K, M;
   int tiles_per_rank;             // W / 128
+  // Device-resident parity (see GatherArgs): box[] then points at parity 0 and
+  // parity p adds p * parity_stride_words 32-bit words.
+  const int* dev_parity;
+  int* arrivals;
+  size_t parity_stride_words;
 };
 
 // Host-side description of one fused call.
@@ -86,6 +102,9 @@ struct FusedLaunch {
   int* status;
   unsigned long long timeout_ns;
   int tp, W, K, M;
+  const int* dev_parity = nullptr;  // device-resident parity (nullptr: box[] resolved)
+  int* arrivals = nullptr;
+  size_t parity_stride_words = 0;
 };
 
 // Limits of the fused path: TP, rows, K granularity, W granularity.

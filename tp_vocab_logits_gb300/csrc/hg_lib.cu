@@ -32,6 +32,7 @@ struct hg_handle {
   int skip_rank = -1;
   bool failed = false;       // hg_sync saw a device error; cleared by hg_rearm
   bool cooperative = false;  // cooperative launch instead of programmatic dependent launch
+  bool device_parity = false;  // parity lives in the status block; calls may be captured
   std::vector<hg::LaunchShape> shape;  // launch shape per M (index M)
   std::vector<int> chunks;             // units per rank-row per M
 };
@@ -157,6 +158,7 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
   }
   h->timeout_ns = opt && opt->poll_timeout_ns ? opt->poll_timeout_ns : kDefaultTimeoutNs;
   h->cooperative = opt && opt->cooperative;
+  h->device_parity = opt && opt->device_parity;
 
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -217,13 +219,21 @@ int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs
     a.shard[r] = shard_ptrs[r];
     a.out[r] = out_ptrs[r];
   }
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return HG_ERR_CUDA;
-  if (cs != cudaStreamCaptureStatusNone) return HG_ERR_CAPTURE;
+  if (!h->device_parity) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return HG_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return HG_ERR_CAPTURE;
+  }
 
   const size_t esz = h->vec16 ? 16 : 4;
+  const int host_parity = h->device_parity ? 0 : h->parity;
   for (int d = 0; d < h->tp; ++d)
-    a.box[d] = static_cast<char*>(h->box[d]) + (size_t)h->parity * h->parity_elems * esz;
+    a.box[d] = static_cast<char*>(h->box[d]) + (size_t)host_parity * h->parity_elems * esz;
+  if (h->device_parity) {
+    a.dev_parity = h->status + hg::kParityWord;
+    a.arrivals = h->status + hg::kArrivalsWord;
+    a.parity_stride = h->parity_elems;
+  }
   for (int d = h->tp; d < HG_MAX_TP; ++d) {
     a.shard[d] = nullptr;
     a.out[d] = nullptr;
@@ -238,7 +248,7 @@ int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs
   a.skip_rank = h->skip_rank;
   if (hg::launch_gather(a, h->shape[M], h->vec16, stream, h->cooperative) != cudaSuccess)
     return HG_ERR_CUDA;
-  h->parity ^= 1;
+  if (!h->device_parity) h->parity ^= 1;
   return HG_OK;
 }
 
@@ -248,6 +258,7 @@ int hg_sync(hg_handle* h, hg_stream_t stream) {
   if (cudaMemcpyAsync(st, h->status, sizeof st, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return HG_ERR_CUDA;
+  if (h->device_parity) h->parity = st[hg::kParityWord] & 1;
   if (st[0] == hg::kDevOk) return HG_OK;
   h->failed = true;
   return HG_ERR_TIMEOUT;
@@ -310,17 +321,25 @@ int hg_gather_fused(hg_handle* h, const void* const* hidden_ptrs, const void* co
       return HG_ERR_ARG;
     if (logits_ptrs && logits_ptrs[r] && !aligned(logits_ptrs[r], 4)) return HG_ERR_ARG;
   }
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return HG_ERR_CUDA;
-  if (cs != cudaStreamCaptureStatusNone) return HG_ERR_CAPTURE;
+  if (!h->device_parity) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return HG_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return HG_ERR_CAPTURE;
+  }
 
   hg::fused::FusedLaunch l;
   l.hidden = hidden_ptrs;
   l.weight = weight_ptrs;
   l.logits = logits_ptrs;
   l.out = out_ptrs;
+  const int host_parity = h->device_parity ? 0 : h->parity;
   for (int d = 0; d < h->tp; ++d)
-    l.box[d] = static_cast<char*>(h->box[d]) + (size_t)h->parity * h->parity_elems * 16;
+    l.box[d] = static_cast<char*>(h->box[d]) + (size_t)host_parity * h->parity_elems * 16;
+  if (h->device_parity) {
+    l.dev_parity = h->status + hg::kParityWord;
+    l.arrivals = h->status + hg::kArrivalsWord;
+    l.parity_stride_words = h->parity_elems * 4;  // 16-byte elements
+  }
   l.status = h->status;
   l.timeout_ns = h->timeout_ns;
   l.tp = h->tp;
@@ -328,7 +347,7 @@ int hg_gather_fused(hg_handle* h, const void* const* hidden_ptrs, const void* co
   l.K = K;
   l.M = M;
   if (hg::fused::fused_launch(l, stream, h->sms) != cudaSuccess) return HG_ERR_CUDA;
-  h->parity ^= 1;
+  if (!h->device_parity) h->parity ^= 1;
   return HG_OK;
 }
 

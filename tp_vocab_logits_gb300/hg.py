@@ -29,7 +29,8 @@ class HGError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("poll_timeout_ns", ctypes.c_uint64), ("elems_per_lane", ctypes.c_int),
-                ("ctas", ctypes.c_int), ("poll_mode", ctypes.c_int), ("cooperative", ctypes.c_int)]
+                ("ctas", ctypes.c_int), ("poll_mode", ctypes.c_int), ("cooperative", ctypes.c_int),
+                ("device_parity", ctypes.c_int)]
 
 
 _LIB: ctypes.CDLL | None = None
@@ -121,13 +122,15 @@ class Handle:
 
 def hg_create(tp: int, shard_cols: int, cap: int, rows: Sequence[int] | None = None, *,
               poll_timeout_ns: int = 0, elems_per_lane: int = 0, ctas: int = 0,
-              poll_mode: int = 0, cooperative: bool = False) -> Handle:
+              poll_mode: int = 0, cooperative: bool = False,
+              device_parity: bool = False) -> Handle:
     lib = load()
     rows = list(rows or [])
     arr = (ctypes.c_int * max(1, len(rows)))(*rows)
     out = ctypes.c_void_p()
-    if poll_timeout_ns or elems_per_lane or ctas or poll_mode or cooperative:
-        opt = _Options(poll_timeout_ns, elems_per_lane, ctas, poll_mode, int(bool(cooperative)))
+    if poll_timeout_ns or elems_per_lane or ctas or poll_mode or cooperative or device_parity:
+        opt = _Options(poll_timeout_ns, elems_per_lane, ctas, poll_mode, int(bool(cooperative)),
+                       int(bool(device_parity)))
         st = lib.hg_create_ex(tp, shard_cols, cap, arr, len(rows), ctypes.byref(opt),
                               ctypes.byref(out))
     else:
