@@ -6,8 +6,8 @@
  * "vllm.models.kimi_k3.nvidia.specialized_decode.runtime.logits_gather",
  * module docstring and class HeadGather): each of TP ranks holds an [M, W]
  * BF16 logits shard (W = V / TP vocab columns). Seen as 32-bit words, rank r's
- * row m is pushed into row m of EVERY rank's mailbox at word columns
- * r * W / 2 ... (the rank-order layout of NCCL's all-gather). A mailbox word
+ * row m is stored into the same row of each rank's mailbox (the pushing rank's
+ * own included), starting at word column r * W / 2: NCCL's all-gather order. A mailbox word
  * that has not arrived holds the sentinel, the BF16 pair (+0, -0) = 0x80000000
  * (low half +0, high half -0); a data word equal to the sentinel is sent as
  * (+0, +0) = 0x00000000, every other word moves unchanged. Each rank polls its
@@ -49,10 +49,10 @@ typedef struct hg_handle hg_handle;
 enum {
   HG_OK = 0,
   HG_ERR_ARG = 1,      /* invalid argument: NULL, misaligned, out of range */
-  HG_ERR_ROWS = 2,     /* row count M not served by this handle (the page's
-                          HeadGather.__call__ "take stock" branch) */
-  HG_ERR_CAPTURE = 3,  /* stream is capturing a CUDA graph (the class
-                          docstring: calls under a graph capture take stock) */
+  HG_ERR_ROWS = 2,     /* row count M not served by this handle (where
+                          HeadGather.__call__ falls back to the stock gather) */
+  HG_ERR_CAPTURE = 3,  /* stream is capturing a CUDA graph (HeadGather also
+                          falls back to the stock gather under capture) */
   HG_ERR_CUDA = 4,     /* a CUDA runtime call failed (allocation, launch) */
   HG_ERR_TIMEOUT = 5,  /* a poll gave up: some pushed word never arrived */
   HG_ERR_STATE = 6     /* the handle holds an unrecovered device error;

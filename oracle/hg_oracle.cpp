@@ -19,8 +19,9 @@
 //    in the high half, so the word is 0x80000000.
 //  * Only a data word exactly equal to the sentinel is rewritten, to the pair
 //    (+0, +0) = 0x00000000. Every other word moves unchanged.
-//  * The rank's own fragment also goes through its own mailbox ("row m of
-//    every rank's mailbox"), so all TP outputs are identical.
+//  * The rank's own fragment also goes through its own mailbox (the push
+//    targets every rank, the pushing rank included), so all TP outputs are
+//    identical.
 //  * Parity starts at 0 and flips on every served call; a call whose row count
 //    is not served returns before the flip and changes nothing.
 //  * The LM head multiplies hidden [M, K] by the rank's weight held in the
@@ -121,8 +122,9 @@ const uint32_t* og_mailbox(const void* h, int d, int q) {
 // the module docstring).
 //   shard: [tp][M][w] words, rank r's [M, W] bf16 logits viewed as int32.
 //   out:   [tp][M][tp * w] words, rank d's [M, V] bf16 output.
-// Returns 0 on success; -1 when M is not served (no state change, the page's
-// "take stock" branch); -2 when some polled word is still the sentinel (the
+// Returns 0 on success; -1 when M is not served (no state change: the page's
+// call falls back to its stock gather there); -2 when some polled word is still
+// the sentinel (the
 // poll would never finish; cannot happen when every rank pushes).
 int og_call(void* h, int M, const uint32_t* shard, uint32_t* out) {
   OracleGather* g = static_cast<OracleGather*>(h);
