@@ -255,18 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   const int lane = (int)threadIdx.x & 31;
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  size_t parity_off = 0;  // in 32-bit words
-  if (a.dev_parity) {
-    // Device-resident parity: read by every thread, flipped by the last CTA
-    // to arrive (after every CTA has read it).
-    const int p = ld_relaxed_s32(a.dev_parity);
-    parity_off = (size_t)p * a.parity_stride_words;
-    __syncthreads();
-    if (threadIdx.x == 0 && atomicAdd(a.arrivals, 1) == (int)gridDim.x - 1) {
-      atomicExch(a.arrivals, 0);
-      atomicExch(const_cast<int*>(a.dev_parity), p ^ 1);
-    }
-  }
+  // Device-resident parity: this CTA's copy g (every thread reads it; the CTA
+  // flips its share of the copies once every thread is past this point).
+  int parity = 0;
+  if (a.parity_words) parity = ld_relaxed_s32(a.parity_words + blockIdx.x);
+  const size_t parity_off = (size_t)parity * a.parity_stride_words;  // in 32-bit words
   if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
 
   if (threadIdx.x == 0) {
@@ -405,6 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const bool failed = sh->failed != 0;
+  if (a.parity_words && !failed) {
+    // Every thread of this CTA read copy g before the barriers above: flip
+    // copies g + k * G (each copy flips exactly once per call).
+    for (int e = (int)blockIdx.x + (int)threadIdx.x * (int)gridDim.x; e < a.parity_entries;
+         e += kThreads * (int)gridDim.x)
+      asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(a.parity_words + e),
+                   "r"(parity ^ 1)
+                   : "memory");
+  }
   if (failed) {
     // Let in-flight TMA copies and MMAs land before the CTA's memory goes.
     const unsigned long long t0 = globaltimer_ns();
@@ -519,8 +521,8 @@ cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   }
   a.status = l.status;
   a.timeout_ns = l.timeout_ns;
-  a.dev_parity = l.dev_parity;
-  a.arrivals = l.arrivals;
+  a.parity_words = l.parity_words;
+  a.parity_entries = l.parity_entries;
   a.parity_stride_words = l.parity_stride_words;
   a.tp = l.tp;
   a.W = l.W;

@@ -242,39 +242,57 @@ template <typename V, int VPT, bool PIPE, bool STREAM, int MAXT>
 __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
   // Programmatic dependent launch: wait until the previous kernel on the
-  // stream has completed and its memory is visible, then let the next kernel
-  // start launching. Nothing is read or written before the wait.
+  // stream has completed and its memory is visible. Nothing is read or
+  // written before the wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int lane = (int)threadIdx.x & 31;
   const int d = (int)threadIdx.x >> 5;  // this warp's rank: mailbox and output
-  size_t parity_off = 0;
-  if (a.dev_parity) {
-    // Device-resident parity: every thread reads it, then the last CTA to
-    // arrive flips it for the next call (no CTA can read it after the flip).
-    const int p = ld_relaxed_s32(a.dev_parity);
-    parity_off = (size_t)p * a.parity_stride;
-    __syncthreads();
-    if (threadIdx.x == 0 && atomicAdd(a.arrivals, 1) == (int)gridDim.x - 1) {
-      atomicExch(a.arrivals, 0);
-      atomicExch(const_cast<int*>(a.dev_parity), p ^ 1);
-    }
-  }
-  // One load per warp of one address: every lane sees the same value.
-  if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
-
   const int N = a.M * a.tp * a.chunks;  // units
   const int G = (int)gridDim.x;
   const int g = (int)blockIdx.x;
   const int cons = (g + 1 == G) ? 0 : g + 1;  // the CTA whose pushes we consume
   const int iters = (N + G - 1) / G;
-  V* const box = reinterpret_cast<V*>(a.box[d]) + parity_off;
+
+  // The first push's shard loads do not depend on the parity: start them
+  // before anything else, so that their latency overlaps the parity and
+  // status reads.
+  V x0[VPT];
+  UnitPos p0{};
+  const bool push0 = iters > 0 && g < N;
+  if (push0) {
+    p0 = unit_pos<VPT>(a, g, lane);
+    if (p0.r != a.skip_rank) {
+      const V* src = reinterpret_cast<const V*>(a.shard[p0.r]) + p0.src;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v)
+        if (p0.idx + 32 * v < a.wv) x0[v] = E::ld_shard(src + 32 * v);
+    }
+  }
+  // Device-resident parity: this warp's own copy (one load per warp of one
+  // address, so every lane sees the same value).
+  const int reader = g * a.tp + d;
+  int parity = 0;
+  if (a.parity_words) parity = ld_relaxed_s32(a.parity_words + reader);
+  // Let the next kernel on the stream start launching (it waits for this one
+  // to complete before it touches memory).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // One load per warp of one address: every lane sees the same value.
+  if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
+
+  V* const box = reinterpret_cast<V*>(a.box[d]) + (size_t)parity * a.parity_stride;
   V* const out = reinterpret_cast<V*>(a.out[d]);
+
+  // Iteration 0's push, from the loads started above.
+  if (push0 && p0.r != a.skip_rank) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+      if (p0.idx + 32 * v < a.wv) E::st_relaxed(box + p0.dst + 32 * v, E::rewrite(x0[v]));
+  }
 
   for (int t = 0; t <= iters; ++t) {
     const int up = t * G + g;
-    if (t < iters && up < N) {
+    if (t >= 1 && t < iters && up < N) {
       const UnitPos p = unit_pos<VPT>(a, up, lane);
       if (p.r != a.skip_rank) {
         const V* src = reinterpret_cast<const V*>(a.shard[p.r]) + p.src;
@@ -300,6 +318,17 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
         }
       }
     }
+  }
+  if (a.parity_words) {
+    // Flip this warp's share of the parity copies: copies reader + k * G * tp,
+    // so that every copy flips exactly once per call whatever the grid size.
+    // None of them but this warp's own is read in this call, and that one was
+    // read above by this warp.
+    const int stride = G * a.tp;
+    for (int e = reader + lane * stride; e < a.parity_entries; e += 32 * stride)
+      asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(a.parity_words + e),
+                   "r"(parity ^ 1)
+                   : "memory");
   }
 }
 

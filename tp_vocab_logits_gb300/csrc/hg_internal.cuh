@@ -18,12 +18,8 @@ constexpr uint32_t kSentinel = 0x80000000u;
 constexpr uint32_t kSentAs = 0x00000000u;
 
 // Device status block. status[0]: kDevOk or kDevTimeout; status[1..3]: where
-// a poll gave up (unit index, consumer rank, first word offset);
-// status[kParityWord]: the parity of handles whose parity lives on the device;
-// status[kArrivalsWord]: CTAs of the current call that have read it.
+// a poll gave up (unit index, consumer rank, first word offset).
 enum DevStatus : int { kDevOk = 0, kDevTimeout = 1 };
-constexpr int kParityWord = 4;
-constexpr int kArrivalsWord = 5;
 constexpr int kStatusWords = 8;
 
 // Arguments of one gather launch. Element = 16-byte vector (vector path) or
@@ -40,11 +36,13 @@ struct GatherArgs {
   int chunks;     // units per rank-row: ceil(wv / (32 * vpt))
   int skip_rank;  // test hook: rank whose push is skipped (-1: none)
   // Device-resident parity: nullptr when box[] already points at the parity in
-  // use; otherwise box[] points at parity 0, parity p adds p * parity_stride
-  // elements, and the kernel reads the parity from here and flips it once
-  // every CTA has read it (arrivals counts them).
-  const int* dev_parity = nullptr;
-  int* arrivals = nullptr;
+  // use. Otherwise box[] points at parity 0, parity p adds p * parity_stride
+  // elements, and parity_words holds parity_entries copies of the parity.
+  // Warp d of CTA g reads copy g * tp + d; when done it flips copies
+  // g * tp + d + k * G * tp, so every copy flips exactly once per call for any
+  // grid size, with no coordination between CTAs.
+  int* parity_words = nullptr;
+  int parity_entries = 0;
   size_t parity_stride = 0;
 };
 
@@ -86,9 +84,10 @@ struct FusedArgs {
   int tp, W, K, M;
   int tiles_per_rank;             // W / 128
   // Device-resident parity (see GatherArgs): box[] then points at parity 0 and
-  // parity p adds p * parity_stride_words 32-bit words.
-  const int* dev_parity;
-  int* arrivals;
+  // parity p adds p * parity_stride_words 32-bit words; CTA g reads copy g and
+  // flips copies g + k * G.
+  int* parity_words;
+  int parity_entries;
   size_t parity_stride_words;
 };
 
@@ -102,8 +101,8 @@ struct FusedLaunch {
   int* status;
   unsigned long long timeout_ns;
   int tp, W, K, M;
-  const int* dev_parity = nullptr;  // device-resident parity (nullptr: box[] resolved)
-  int* arrivals = nullptr;
+  int* parity_words = nullptr;  // device-resident parity copies (nullptr: box[] resolved)
+  int parity_entries = 0;
   size_t parity_stride_words = 0;
 };
 

@@ -32,7 +32,9 @@ struct hg_handle {
   int skip_rank = -1;
   bool failed = false;       // hg_sync saw a device error; cleared by hg_rearm
   bool cooperative = false;  // cooperative launch instead of programmatic dependent launch
-  bool device_parity = false;  // parity lives in the status block; calls may be captured
+  bool device_parity = false;  // parity lives on the device; calls may be captured
+  int* parity_words = nullptr;  // copies of the device-resident parity
+  int parity_entries = 0;
   std::vector<hg::LaunchShape> shape;  // launch shape per M (index M)
   std::vector<int> chunks;             // units per rank-row per M
 };
@@ -50,6 +52,7 @@ void free_handle(hg_handle* h) {
   for (int d = 0; d < HG_MAX_TP; ++d)
     if (h->box[d]) cudaFree(h->box[d]);
   if (h->status) cudaFree(h->status);
+  if (h->parity_words) cudaFree(h->parity_words);
   delete h;
 }
 
@@ -184,6 +187,19 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
       return HG_ERR_CUDA;
     }
   }
+  if (h->device_parity) {
+    // One copy per reader: warp d of CTA g of a gather reads copy g * tp + d,
+    // CTA g of a fused call (at most one CTA per SM) reads copy g.
+    int max_ctas = 0;
+    for (int M = 1; M <= cap; ++M)
+      if (h->served[M] && h->shape[M].ctas > max_ctas) max_ctas = h->shape[M].ctas;
+    h->parity_entries = max_ctas * tp > h->sms ? max_ctas * tp : h->sms;
+    if (cudaMalloc(&h->parity_words, (size_t)h->parity_entries * sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->parity_words, 0, (size_t)h->parity_entries * sizeof(int)) != cudaSuccess) {
+      free_handle(h);
+      return HG_ERR_CUDA;
+    }
+  }
   if (cudaMalloc(&h->status, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
       cudaMemset(h->status, 0, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
@@ -230,8 +246,8 @@ int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs
   for (int d = 0; d < h->tp; ++d)
     a.box[d] = static_cast<char*>(h->box[d]) + (size_t)host_parity * h->parity_elems * esz;
   if (h->device_parity) {
-    a.dev_parity = h->status + hg::kParityWord;
-    a.arrivals = h->status + hg::kArrivalsWord;
+    a.parity_words = h->parity_words;
+    a.parity_entries = h->parity_entries;
     a.parity_stride = h->parity_elems;
   }
   for (int d = h->tp; d < HG_MAX_TP; ++d) {
@@ -255,10 +271,13 @@ int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs
 int hg_sync(hg_handle* h, hg_stream_t stream) {
   if (!h) return HG_ERR_ARG;
   int st[hg::kStatusWords] = {};
+  int par = 0;
   if (cudaMemcpyAsync(st, h->status, sizeof st, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      (h->device_parity && cudaMemcpyAsync(&par, h->parity_words, sizeof par,
+                                           cudaMemcpyDeviceToHost, stream) != cudaSuccess) ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return HG_ERR_CUDA;
-  if (h->device_parity) h->parity = st[hg::kParityWord] & 1;
+  if (h->device_parity) h->parity = par & 1;
   if (st[0] == hg::kDevOk) return HG_OK;
   h->failed = true;
   return HG_ERR_TIMEOUT;
@@ -271,6 +290,10 @@ int hg_rearm(hg_handle* h, hg_stream_t stream) {
                             stream) != cudaSuccess)
       return HG_ERR_CUDA;
   if (cudaMemsetAsync(h->status, 0, hg::kStatusWords * sizeof(int), stream) != cudaSuccess)
+    return HG_ERR_CUDA;
+  if (h->parity_words &&
+      cudaMemsetAsync(h->parity_words, 0, (size_t)h->parity_entries * sizeof(int), stream) !=
+          cudaSuccess)
     return HG_ERR_CUDA;
   h->parity = 0;
   h->failed = false;
@@ -336,8 +359,8 @@ int hg_gather_fused(hg_handle* h, const void* const* hidden_ptrs, const void* co
   for (int d = 0; d < h->tp; ++d)
     l.box[d] = static_cast<char*>(h->box[d]) + (size_t)host_parity * h->parity_elems * 16;
   if (h->device_parity) {
-    l.dev_parity = h->status + hg::kParityWord;
-    l.arrivals = h->status + hg::kArrivalsWord;
+    l.parity_words = h->parity_words;
+    l.parity_entries = h->parity_entries;
     l.parity_stride_words = h->parity_elems * 4;  // 16-byte elements
   }
   l.status = h->status;
