@@ -61,6 +61,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.og_slice_bf16.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p]
     lib.og_lm_head_f64.argtypes = [_u16p, _u16p, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, _f64p]
+    lib.og_row_stats.argtypes = [_u16p, ctypes.c_int, _f64p, _i32p, _f64p]
     return lib
 
 
@@ -150,3 +151,13 @@ def lm_head_f64(hidden_bits: np.ndarray, weight_bits: np.ndarray, n0: int = 0,
     (lib or _lib()).og_lm_head_f64(h.ctypes.data_as(_u16p), wt.ctypes.data_as(_u16p), M, K,
                                    n0, n1, res.ctypes.data_as(_f64p))
     return res
+
+
+def row_stats(row_bits: np.ndarray, lib=None) -> tuple:
+    """(max_logit, argmax, sum_exp) of one gathered bf16 row (uint16 bits)."""
+    r = np.ascontiguousarray(row_bits, dtype=np.uint16)
+    mx, s = ctypes.c_double(), ctypes.c_double()
+    arg = ctypes.c_int()
+    (lib or _lib()).og_row_stats(r.ctypes.data_as(_u16p), r.shape[0], ctypes.byref(mx),
+                                 ctypes.byref(arg), ctypes.byref(s))
+    return mx.value, arg.value, s.value

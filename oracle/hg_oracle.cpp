@@ -29,11 +29,14 @@
 //    width), i.e. logits[m][n] = sum_k hidden[m][k] * weight[n][k].
 //
 // Parity pinned by the tests: invariants I1-I7, an exhaustive brute force at
-// TP=2, V=8, a hand-worked example, and for the LM head closed forms and a
-// library float64 matmul. No function here is "parity unpinned".
+// TP=2, V=8, a hand-worked example; for the LM head closed forms and a library
+// float64 matmul; for the row statistics numpy/scipy, closed forms and a
+// hand-worked row. No function here is "parity unpinned".
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <limits>
 #include <vector>
 
 namespace {
@@ -173,6 +176,31 @@ void og_slice_bf16(const uint16_t* out, int M, int V, int v_real, uint16_t* slic
   for (int m = 0; m < M; ++m)
     for (int c = 0; c < v_real; ++c)
       sliced[(size_t)m * v_real + c] = out[(size_t)m * V + c];
+}
+
+// Sampler statistics of one gathered row. The API page's module docstring
+// notes that the sentinel rewrite changes no value a sampler computes with
+// (+0 and -0 compare, add and exponentiate alike); these are such values.
+// Over the V bf16 values x_c of the row,
+//   max_logit = max_c x_c
+//   argmax    = the smallest c with x_c == max_logit
+//   sum_exp   = sum over c with x_c != -inf of exp(x_c - max_logit)
+// in double precision. A row of only -inf values has sum_exp 0.
+void og_row_stats(const uint16_t* row, int V, double* max_logit, int* argmax, double* sum_exp) {
+  double mx = -std::numeric_limits<double>::infinity();
+  int arg = 0;
+  for (int c = 0; c < V; ++c) {
+    double x = bf16_to_double(row[c]);
+    if (x > mx) { mx = x; arg = c; }
+  }
+  double s = 0.0;
+  for (int c = 0; c < V; ++c) {
+    double x = bf16_to_double(row[c]);
+    if (x != -std::numeric_limits<double>::infinity()) s += std::exp(x - mx);
+  }
+  *max_logit = mx;
+  *argmax = arg;
+  *sum_exp = s;
 }
 
 // Vocab-parallel LM head of one rank, in double precision:

@@ -12,7 +12,8 @@ numbers, so the oracle is pinned by:
     concatenate), exact sentinel positions, re-armed mailboxes, the parity
     sequence and rejected calls, identical outputs on every rank, an
     exhaustive brute force at TP=2, V=8, and the padded-vocab slice;
-  * for the LM head: one-hot closed forms, K=1, and numpy's float64 matmul.
+  * for the LM head: one-hot closed forms, K=1, and numpy's float64 matmul;
+  * for the row statistics: numpy/scipy, closed forms and a hand-worked row.
 Every check runs against the real oracle and against mutants of it with a
 planted mistake (compiled from a patched copy of the source); each mutant must
 fail at least one check.
@@ -239,10 +240,34 @@ def check_lm_head_matmul(lib):
     np.testing.assert_array_equal(part, out[:, 5:17])
 
 
+def check_row_stats(lib):
+    """Sampler statistics: against numpy/scipy on random rows (max, first
+    argmax, logsumexp), closed forms (a constant row: sum_exp = V, argmax 0),
+    ties resolved to the smallest index, -inf pads excluded from the sum, and
+    a hand-worked row."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(17)
+    for V in (1, 7, 64, 1000):
+        bits = _bf16_bits(rng.standard_normal(V) * 3)
+        vals = _bf16_vals(bits)
+        mx, arg, se = oracle.row_stats(bits, lib=lib)
+        assert mx == vals.max() and arg == int(np.argmax(vals))
+        np.testing.assert_allclose(mx + np.log(se), logsumexp(vals), rtol=1e-13, atol=1e-13)
+    mx, arg, se = oracle.row_stats(_bf16_bits(np.full(50, 1.5)), lib=lib)
+    assert (mx, arg, se) == (1.5, 0, 50.0)
+    assert oracle.row_stats(_bf16_bits(np.array([0.0, 2.0, -1.0, 2.0])), lib=lib)[1] == 1
+    # hand-worked: [0.69140625, -inf, +0]: max at 0, sum = 1 + exp(-0.69140625)
+    mx, arg, se = oracle.row_stats(np.array([0x3F31, 0xFF80, 0x0000], dtype=np.uint16), lib=lib)
+    assert mx == 0.69140625 and arg == 0
+    assert abs(se - (1.0 + np.exp(-0.69140625))) < 1e-15
+    mx, arg, se = oracle.row_stats(np.array([0xFF80, 0xFF80], dtype=np.uint16), lib=lib)
+    assert mx == -np.inf and arg == 0 and se == 0.0
+
+
 CHECKS = [check_sentinel, check_worked_example, check_config1_golden,
           check_concat_without_sentinels, check_sentinel_positions, check_rearm_and_parity,
           check_identical_outputs, check_brute_force_tp2_v8, check_slice,
-          check_lm_head_one_hot, check_lm_head_matmul]
+          check_lm_head_one_hot, check_lm_head_matmul, check_row_stats]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)
@@ -283,6 +308,8 @@ MUTANTS = {
     "lm_head_dropped_term": ("for (int k = 0; k < K; ++k)", "for (int k = 1; k < K; ++k)"),
     "bf16_widening_shift": ("(uint32_t)bits << 16", "(uint32_t)bits << 15"),
     "slice_wrong_stride": ("out[(size_t)m * V + c]", "out[(size_t)m * v_real + c]"),
+    "stats_last_argmax": ("if (x > mx) { mx = x; arg = c; }", "if (x >= mx) { mx = x; arg = c; }"),
+    "stats_sum_without_shift": ("s += std::exp(x - mx);", "s += std::exp(x);"),
 }
 
 
