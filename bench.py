@@ -356,6 +356,40 @@ def run_ours(args):
     ms_max, us_call = replica_us_per_call(dist, ms, args.steps, world, device)
     us_launch = ms * 1000.0 / args.steps  # this rank's average launch duration
 
+    # ---- the same workload with row statistics, and with device parity ----
+    stats_us = devpar_us = torch_stats_us = None
+    if not args.quick:
+        import ctypes
+        st_buf = hg.new_row_stats(M_STEP)
+        lib = hg.load()
+        sp_ = stream.cuda_stream
+        arrs = [((ctypes.c_void_p * TP)(*[shards[s_, r].data_ptr() for r in range(TP)]),
+                 (ctypes.c_void_p * TP)(*[outs[s_, d].data_ptr() for d in range(TP)]))
+                for s_ in range(nsets)]
+        stp = st_buf.data_ptr()
+        fns = [lambda a_=a_: lib.hg_gather_stats(h.ptr, a_[0], a_[1], M_STEP, stp, sp_)
+               for a_ in arrs]
+        t = time_calls(torch, fns, args.steps, args.warmup, stream, "timed_stats")
+        hg.hg_sync(h)
+        stats_us = round(t * 1000.0 / args.steps, 3)
+
+        def gather_then_torch(i=[0]):  # the unfused alternative
+            calls[i[0] % nsets]()
+            row = outs[i[0] % nsets, 0].view(torch.bfloat16).float()
+            torch.max(row, dim=1)
+            torch.logsumexp(row, dim=1)
+            i[0] += 1
+        t = time_calls(torch, [gather_then_torch], 200, args.warmup, stream, "timed_torch_stats")
+        hg.hg_sync(h)
+        torch_stats_us = round(t * 1000.0 / 200, 3)
+        hdp, sdp, odp, cdp = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device,
+                                           device_parity=True)
+        t = time_calls(torch, cdp, args.steps, args.warmup, stream, "timed_devparity")
+        hg.hg_sync(hdp)
+        devpar_us = round(t * 1000.0 / args.steps, 3)
+        hdp.close()
+        del sdp, odp, cdp
+
     # ---- the same calls captured in a CUDA graph (device-resident parity) ----
     graph_us = None
     if not args.quick:
@@ -492,6 +526,9 @@ def run_ours(args):
                              "L2-resident and the launch is latency-bound"},
         "per_m": per_m,
         "large_m": large,
+        "with_row_stats_us_per_call": stats_us,
+        "gather_then_torch_row_stats_us_per_call": torch_stats_us,
+        "device_parity_us_per_call": devpar_us,
         "graph_replay_us_per_call": graph_us,
         "stock_memcpy2d_us_per_call": stock_us,
         "fused_lm_head": fused,

@@ -257,6 +257,31 @@ int hg_stock_gather(int tp, int shard_cols, const void *const *shard_ptrs,
 int hg_gather_static(int tp, int shard_cols, const void *const *shard_ptrs,
                      void *const *out_ptrs, int M, int *status_out, hg_stream_t stream);
 
+/* Sampler statistics of one gathered row (over its V bf16 values x_c). */
+typedef struct hg_row_stats {
+  float max_logit;  /* max_c x_c */
+  int argmax;       /* smallest c with x_c == max_logit */
+  float sum_exp;    /* sum of exp(x_c - max_logit) over x_c != -inf */
+  float logsumexp;  /* max_logit + log(sum_exp) */
+} hg_row_stats;
+
+/*
+ * hg_gather_stats - hg_gather plus sampler statistics of every gathered row,
+ * folded by the pollers while they copy. The API page's module docstring
+ * notes that the sentinel rewrite leaves every value a sampler uses
+ * unchanged, so these are the sampler's statistics of the gathered row. Same
+ * arguments, contract and errors as hg_gather (tp <= 16), plus
+ *
+ *   stats  device pointer to M hg_row_stats, written in stream order: for
+ *          row m, over its V = tp * W bf16 values x_c (rank-order columns),
+ *          max_logit = max x_c, argmax = the smallest c attaining it,
+ *          sum_exp = sum of exp(x_c - max_logit) over x_c != -inf (fp32,
+ *          any summation order), logsumexp = max_logit + log(sum_exp).
+ *          Rows holding NaN or +inf give unspecified statistics.
+ */
+int hg_gather_stats(hg_handle *h, const void *const *shard_ptrs, void *const *out_ptrs, int M,
+                    hg_row_stats *stats, hg_stream_t stream);
+
 /* Human-readable text of a status code; never NULL. */
 const char *hg_strerror(int status);
 

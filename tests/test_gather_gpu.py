@@ -107,6 +107,17 @@ def test_launch_shapes_vs_oracle(vpt, ctas, mode, coop):
                  cooperative=coop)
 
 
+def test_multi_wave_decode_width_vs_oracle():
+    """TP8, V=163840, M=64: more units than co-resident CTAs, so every CTA loops
+    over units with simple polls; three calls (both parities) against the
+    oracle word for word."""
+    tp, W, M = 8, 20480, 64
+    h = hg.hg_create(tp, W, M)
+    assert not hg.hg_launch_shape(h, M)["pipelined"]
+    h.close()
+    run_sequence(tp, W, M, [M, M, M])
+
+
 @pytest.mark.parametrize("tp", [24, 32])
 def test_wide_tp_vs_oracle(tp):
     """TP above 16 runs 1024-thread CTAs (one warp per rank)."""

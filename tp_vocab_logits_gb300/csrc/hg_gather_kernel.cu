@@ -67,6 +67,10 @@ struct Elem;
 // 16-byte vector of four words.
 template <>
 struct Elem<uint4> {
+  static constexpr int kWords = 4;
+  static __device__ __forceinline__ uint32_t word(const uint4& v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+  }
   static __device__ __forceinline__ uint4 ld_shard(const uint4* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -109,6 +113,8 @@ struct Elem<uint4> {
 // One 32-bit word (shards whose width is not a multiple of 8 columns).
 template <>
 struct Elem<uint32_t> {
+  static constexpr int kWords = 1;
+  static __device__ __forceinline__ uint32_t word(uint32_t v, int) { return v; }
   static __device__ __forceinline__ uint32_t ld_shard(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -235,10 +241,156 @@ __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, con
   return !__any_sync(kFull, gave_up);
 }
 
+// ---- Row statistics (max, first argmax, sum of exp(x - max)) -------------
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr int kCellBatch = 6;  // statistics cells each reducer thread loads at once
+
+// (mx, arg) <- the larger of (mx, arg) and (x, col); ties keep the smaller column.
+__device__ __forceinline__ void max_add(float& mx, int& arg, float x, int col) {
+  if (x > mx || (x == mx && col < arg)) {
+    mx = x;
+    arg = col;
+  }
+}
+
+// (mx, arg, s) <- its combination with (mx2, arg2, s2), where s is a sum of
+// exp(x - mx) over finite x (0 when mx is -inf).
+__device__ __forceinline__ void combine_partial(float& mx, int& arg, float& s, float mx2,
+                                                int arg2, float s2) {
+  const float m = fmaxf(mx, mx2);
+  const int a = mx > mx2 ? arg : (mx2 > mx ? arg2 : min(arg, arg2));
+  float t = 0.f;
+  if (mx != kNegInf) t += s * __expf(mx - m);
+  if (mx2 != kNegInf) t += s2 * __expf(mx2 - m);
+  mx = m;
+  arg = a;
+  s = t;
+}
+
+// Statistics of unit u's values, folded by warp 0 from rank 0's copy (every
+// rank's copy holds the same values). Two passes over registers: the warp's
+// max and first argmax, then the sum of exp(x - max) over finite x. Lane 0
+// writes the result into cell u with one relaxed 16-byte store.
+template <typename V, int VPT>
+__device__ __forceinline__ void unit_stats(const GatherArgs& a, const UnitPos& p, int u,
+                                           const V (&res)[VPT]) {
+  using E = Elem<V>;
+  float mx = kNegInf;
+  int arg = 0x7fffffff;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    if (p.idx + 32 * v < a.wv) {
+      const int col0 = p.r * a.shard_cols + (p.idx + 32 * v) * (2 * E::kWords);
+#pragma unroll
+      for (int k = 0; k < E::kWords; ++k) {
+        const uint32_t w = E::word(res[v], k);
+        max_add(mx, arg, __uint_as_float(w << 16), col0 + 2 * k);
+        max_add(mx, arg, __uint_as_float(w & 0xffff0000u), col0 + 2 * k + 1);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(kFull, mx, off);
+    const int a2 = __shfl_xor_sync(kFull, arg, off);
+    max_add(mx, arg, m2, a2);
+  }
+  float s = 0.f;
+  if (mx != kNegInf) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (p.idx + 32 * v < a.wv) {
+#pragma unroll
+        for (int k = 0; k < E::kWords; ++k) {
+          const uint32_t w = E::word(res[v], k);
+          const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+          if (lo != kNegInf) s += __expf(lo - mx);
+          if (hi != kNegInf) s += __expf(hi - mx);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  if ((threadIdx.x & 31) == 0) {
+    // A Lamport cell: no word may equal the sentinel, so a -0.0 max is
+    // written as +0.0 (the same value); the other words cannot be it.
+    uint4 w;
+    w.x = __float_as_uint(mx) == kSentinel ? 0u : __float_as_uint(mx);
+    w.y = (uint32_t)arg;
+    w.z = __float_as_uint(s);
+    w.w = 1u;
+    Elem<uint4>::st_relaxed(reinterpret_cast<uint4*>(a.partials + u), w);
+  }
+}
+
+// Warp 0 of CTA 0, once its own units are done: poll every row's cells
+// until all have arrived (bounded), fold them, re-arm them and write the [M]
+// statistics. Only warps 0 write cells, so neither a CTA barrier nor any
+// atomic is involved: the cells carry their own arrival, as mailbox words do.
+__device__ __forceinline__ void finish_stats(const GatherArgs& a) {
+  const int lane = (int)threadIdx.x & 31;
+  const int per_row = a.tp * a.chunks;  // cells (units) per row
+  const uint4 armed = make_uint4(kSentinel, kSentinel, kSentinel, kSentinel);
+  for (int m = 0; m < a.M; ++m) {
+    uint4* q = reinterpret_cast<uint4*>(a.partials + (size_t)m * per_row);
+    float mx = kNegInf, s = 0.f;
+    int arg = 0x7fffffff;
+    bool gave_up = false;
+    for (int base = lane; base < per_row; base += kCellBatch * 32) {
+      // Issue a batch of cell loads first, so that their latencies overlap.
+      uint4 v[kCellBatch];
+#pragma unroll
+      for (int k = 0; k < kCellBatch; ++k)
+        if (base + 32 * k < per_row) v[k] = Elem<uint4>::ld_poll(q + base + 32 * k);
+#pragma unroll
+      for (int k = 0; k < kCellBatch; ++k) {
+        const int j = base + 32 * k;
+        if (j >= per_row || gave_up) continue;
+        if (!Elem<uint4>::arrived(v[k])) {
+          const unsigned long long t0 = globaltimer_ns();
+          do {
+            v[k] = Elem<uint4>::ld_poll(q + j);
+            if (Elem<uint4>::arrived(v[k])) break;
+            if (globaltimer_ns() - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+              record_timeout(a, -1, -1, (size_t)j);
+              gave_up = true;
+              break;
+            }
+          } while (true);
+          if (gave_up) continue;
+        }
+        combine_partial(mx, arg, s, __uint_as_float(v[k].x), (int)v[k].y,
+                        __uint_as_float(v[k].z));
+        Elem<uint4>::st_relaxed(q + j, armed);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(kFull, mx, off);
+      const int a2 = __shfl_xor_sync(kFull, arg, off);
+      const float s2 = __shfl_xor_sync(kFull, s, off);
+      combine_partial(mx, arg, s, m2, a2, s2);
+    }
+    if (__any_sync(kFull, gave_up)) return;
+    if (lane == 0) {
+      hg_row_stats r;
+      r.max_logit = mx;
+      r.argmax = arg;
+      r.sum_exp = s;
+      r.logsumexp = mx + logf(s);
+      a.stats[m] = r;
+    }
+  }
+}
+
 // VPT: elements per lane per unit. PIPE: staggered double polls (single-wave
 // launches). STREAM: evict-first stores of the outputs (multi-iteration
 // launches, whose outputs L2 should not keep). MAXT: largest CTA (32 * tp).
-template <typename V, int VPT, bool PIPE, bool STREAM, int MAXT>
+// STATS: warp 0 (rank 0's copy of every row) also folds each consumed unit
+// into a statistics cell, and warp 0 of CTA 0 folds the cells of every row.
+template <typename V, int VPT, bool PIPE, bool STREAM, int MAXT, bool STATS>
 __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
   // Programmatic dependent launch: wait until the previous kernel on the
@@ -317,6 +469,8 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
           E::st_relaxed(box + p.dst + 32 * v, E::sentinel());
         }
       }
+      // After the stores, so that the folding overlaps their completion.
+      if (STATS && d == 0) unit_stats<V, VPT>(a, p, uc, res);
     }
   }
   if (a.parity_words) {
@@ -330,6 +484,7 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
                    "r"(parity ^ 1)
                    : "memory");
   }
+  if (STATS && g == 0 && d == 0) finish_stats(a);  // warp 0 of CTA 0 folds every row's cells
 }
 
 __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
@@ -339,27 +494,34 @@ __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
 }
 
 // Kernels for tp <= 16 (CTAs of up to 512 threads) take 1, 2 or 4 elements
-// per lane; larger tp (up to 1024 threads, 64 registers) 1 or 2.
-template <typename V, bool PIPE>
+// per lane; larger tp (up to 1024 threads, 64 registers) 1 or 2. Row
+// statistics exist for tp <= 16.
+template <typename V, bool PIPE, bool STATS>
 const void* pick_vpt(int vpt, int tp) {
   if (tp <= 16) {
     switch (vpt) {
-      case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 512>);
-      case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 512>);
-      case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4, PIPE, !PIPE, 512>);
+      case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 512, STATS>);
+      case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 512, STATS>);
+      case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4, PIPE, !PIPE, 512, STATS>);
       default: return nullptr;
     }
   }
+  if (STATS) return nullptr;
   switch (vpt) {
-    case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 1024>);
-    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 1024>);
+    case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 1024, false>);
+    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 1024, false>);
     default: return nullptr;
   }
 }
 
+template <typename V, bool PIPE>
+const void* pick_stats(const LaunchShape& s, int tp) {
+  return s.stats ? pick_vpt<V, PIPE, true>(s.vpt, tp) : pick_vpt<V, PIPE, false>(s.vpt, tp);
+}
+
 const void* kernel_for(const LaunchShape& s, bool vec16, int tp) {
-  if (vec16) return s.pipe ? pick_vpt<uint4, true>(s.vpt, tp) : pick_vpt<uint4, false>(s.vpt, tp);
-  return s.pipe ? pick_vpt<uint32_t, true>(s.vpt, tp) : pick_vpt<uint32_t, false>(s.vpt, tp);
+  if (vec16) return s.pipe ? pick_stats<uint4, true>(s, tp) : pick_stats<uint4, false>(s, tp);
+  return s.pipe ? pick_stats<uint32_t, true>(s, tp) : pick_stats<uint32_t, false>(s, tp);
 }
 
 }  // namespace

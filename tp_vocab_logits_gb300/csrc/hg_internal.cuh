@@ -22,6 +22,17 @@ constexpr uint32_t kSentAs = 0x00000000u;
 enum DevStatus : int { kDevOk = 0, kDevTimeout = 1 };
 constexpr int kStatusWords = 8;
 
+// Row statistics of one unit's values (max, first argmax, sum of exp(x -
+// max)), 16 bytes. The cells are Lamport cells: armed with the
+// sentinel in every word, written with relaxed stores (a word equal to the
+// sentinel written as zero, as in the gather), polled and re-armed by CTA 0.
+struct RowPartial {
+  float max;
+  int arg;
+  float sum;
+  int mark;  // 1 once written
+};
+
 // Arguments of one gather launch. Element = 16-byte vector (vector path) or
 // one 32-bit word (word path).
 struct GatherArgs {
@@ -44,6 +55,11 @@ struct GatherArgs {
   int* parity_words = nullptr;
   int parity_entries = 0;
   size_t parity_stride = 0;
+  // Row statistics (kernels built with them only): one cell per unit, the [M]
+  // output, and the shard width in bf16 columns.
+  RowPartial* partials = nullptr;
+  hg_row_stats* stats = nullptr;
+  int shard_cols = 0;
 };
 
 // Launch shape of one row count: CTAs (32 * tp threads each), elements per lane
@@ -52,6 +68,7 @@ struct LaunchShape {
   int ctas = 0;
   int vpt = 1;
   bool pipe = true;
+  bool stats = false;  // the kernel also folds row statistics
 };
 
 // Largest co-resident CTAs per SM of the gather kernel for this shape.

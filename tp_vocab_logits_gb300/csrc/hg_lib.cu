@@ -37,6 +37,10 @@ struct hg_handle {
   int parity_entries = 0;
   std::vector<hg::LaunchShape> shape;  // launch shape per M (index M)
   std::vector<int> chunks;             // units per rank-row per M
+  std::vector<hg::LaunchShape> shape_stats;  // the same for hg_gather_stats (tp <= 16)
+  std::vector<int> chunks_stats;
+  hg::RowPartial* partials = nullptr;  // statistics cells: one per unit of the largest call
+  size_t partial_count = 0;
 };
 
 namespace {
@@ -53,6 +57,7 @@ void free_handle(hg_handle* h) {
     if (h->box[d]) cudaFree(h->box[d]);
   if (h->status) cudaFree(h->status);
   if (h->parity_words) cudaFree(h->parity_words);
+  if (h->partials) cudaFree(h->partials);
   delete h;
 }
 
@@ -65,7 +70,8 @@ void free_handle(hg_handle* h) {
 // the co-resident maximum of the simple kernel, looping over the units. The
 // grid never exceeds the co-resident CTA count, which the kernel's cross-CTA
 // polls need.
-int plan_one(hg_handle* h, int M, const hg_options* opt, hg::LaunchShape* out, int* chunks_out) {
+int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchShape* out,
+             int* chunks_out) {
   const int forced_vpt = opt ? opt->elems_per_lane : 0;
   const int forced_ctas = opt ? opt->ctas : 0;
   const int mode = opt ? opt->poll_mode : 0;
@@ -80,6 +86,7 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, hg::LaunchShape* out, i
     return HG_OK;
   };
   hg::LaunchShape s;
+  s.stats = stats;
   s.vpt = forced_vpt ? forced_vpt : max_vpt;
   const int chunks = (h->wv + 32 * s.vpt - 1) / (32 * s.vpt);
   const long long units = (long long)M * h->tp * chunks;
@@ -103,13 +110,24 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, hg::LaunchShape* out, i
   return HG_OK;
 }
 
+// Shapes of every served M, for hg_gather and (tp <= 16) hg_gather_stats, and
+// the number of statistics cells the largest stats call needs.
 int plan_shapes(hg_handle* h, const hg_options* opt) {
   h->shape.assign(h->cap + 1, hg::LaunchShape());
   h->chunks.assign(h->cap + 1, 0);
+  h->shape_stats.assign(h->cap + 1, hg::LaunchShape());
+  h->chunks_stats.assign(h->cap + 1, 0);
+  h->partial_count = 0;
   for (int M = 1; M <= h->cap; ++M) {
     if (!h->served[M]) continue;
-    int st = plan_one(h, M, opt, &h->shape[M], &h->chunks[M]);
+    int st = plan_one(h, M, opt, false, &h->shape[M], &h->chunks[M]);
     if (st != HG_OK) return st;
+    if (h->tp <= 16) {
+      st = plan_one(h, M, opt, true, &h->shape_stats[M], &h->chunks_stats[M]);
+      if (st != HG_OK) return st;
+      const size_t cells = (size_t)M * h->tp * h->chunks_stats[M];  // one per unit
+      if (cells > h->partial_count) h->partial_count = cells;
+    }
   }
   return HG_OK;
 }
@@ -187,12 +205,23 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
       return HG_ERR_CUDA;
     }
   }
+  if (h->partial_count) {
+    // Statistics cells, armed with the sentinel (Lamport cells).
+    if (cudaMalloc(&h->partials, h->partial_count * sizeof(hg::RowPartial)) != cudaSuccess ||
+        hg::launch_fill_u32(reinterpret_cast<uint32_t*>(h->partials), h->partial_count * 4,
+                            hg::kSentinel, nullptr) != cudaSuccess) {
+      free_handle(h);
+      return HG_ERR_CUDA;
+    }
+  }
   if (h->device_parity) {
     // One copy per reader: warp d of CTA g of a gather reads copy g * tp + d,
     // CTA g of a fused call (at most one CTA per SM) reads copy g.
     int max_ctas = 0;
-    for (int M = 1; M <= cap; ++M)
+    for (int M = 1; M <= cap; ++M) {
       if (h->served[M] && h->shape[M].ctas > max_ctas) max_ctas = h->shape[M].ctas;
+      if (h->served[M] && h->shape_stats[M].ctas > max_ctas) max_ctas = h->shape_stats[M].ctas;
+    }
     h->parity_entries = max_ctas * tp > h->sms ? max_ctas * tp : h->sms;
     if (cudaMalloc(&h->parity_words, (size_t)h->parity_entries * sizeof(int)) != cudaSuccess ||
         cudaMemset(h->parity_words, 0, (size_t)h->parity_entries * sizeof(int)) != cudaSuccess) {
@@ -221,9 +250,12 @@ int hg_destroy(hg_handle* h) {
   return st;
 }
 
-int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
-              hg_stream_t stream) {
+namespace {
+
+int gather_impl(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
+                hg_row_stats* stats, hg_stream_t stream) {
   if (!h || !shard_ptrs || !out_ptrs) return HG_ERR_ARG;
+  if (stats && (h->tp > 16 || !h->partials)) return HG_ERR_ARG;
   if (M < 1 || M > h->cap || !h->served[M]) return HG_ERR_ROWS;
   if (h->failed) return HG_ERR_STATE;
   const size_t align = h->vec16 ? 16 : 4;
@@ -260,12 +292,31 @@ int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs
   a.tp = h->tp;
   a.wv = h->wv;
   a.M = M;
-  a.chunks = h->chunks[M];
+  a.chunks = stats ? h->chunks_stats[M] : h->chunks[M];
   a.skip_rank = h->skip_rank;
-  if (hg::launch_gather(a, h->shape[M], h->vec16, stream, h->cooperative) != cudaSuccess)
+  if (stats) {
+    a.partials = h->partials;
+    a.stats = stats;
+    a.shard_cols = h->W;
+  }
+  const hg::LaunchShape& shape = stats ? h->shape_stats[M] : h->shape[M];
+  if (hg::launch_gather(a, shape, h->vec16, stream, h->cooperative) != cudaSuccess)
     return HG_ERR_CUDA;
   if (!h->device_parity) h->parity ^= 1;
   return HG_OK;
+}
+
+}  // namespace
+
+int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
+              hg_stream_t stream) {
+  return gather_impl(h, shard_ptrs, out_ptrs, M, nullptr, stream);
+}
+
+int hg_gather_stats(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
+                    hg_row_stats* stats, hg_stream_t stream) {
+  if (!stats) return HG_ERR_ARG;
+  return gather_impl(h, shard_ptrs, out_ptrs, M, stats, stream);
 }
 
 int hg_sync(hg_handle* h, hg_stream_t stream) {
@@ -294,6 +345,10 @@ int hg_rearm(hg_handle* h, hg_stream_t stream) {
   if (h->parity_words &&
       cudaMemsetAsync(h->parity_words, 0, (size_t)h->parity_entries * sizeof(int), stream) !=
           cudaSuccess)
+    return HG_ERR_CUDA;
+  if (h->partials &&
+      hg::launch_fill_u32(reinterpret_cast<uint32_t*>(h->partials), h->partial_count * 4,
+                          hg::kSentinel, stream) != cudaSuccess)
     return HG_ERR_CUDA;
   h->parity = 0;
   h->failed = false;

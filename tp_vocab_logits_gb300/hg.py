@@ -64,11 +64,12 @@ def load() -> ctypes.CDLL:
     lib.hg_debug_skip_push.argtypes = [vp, i]
     lib.hg_stock_gather.argtypes = [i, i, vpp, vpp, i, st]
     lib.hg_gather_fused.argtypes = [vp, vpp, vpp, vpp, vpp, i, i, st]
+    lib.hg_gather_stats.argtypes = [vp, vpp, vpp, i, vp, st]
     lib.hg_strerror.argtypes = [i]
     lib.hg_strerror.restype = ctypes.c_char_p
     for name in ("hg_create", "hg_create_ex", "hg_destroy", "hg_gather", "hg_sync", "hg_rearm",
                  "hg_parity", "hg_mailbox", "hg_launch_shape", "hg_debug_skip_push",
-                 "hg_stock_gather", "hg_gather_fused"):
+                 "hg_stock_gather", "hg_gather_fused", "hg_gather_stats"):
         getattr(lib, name).restype = i
     _LIB = lib
     return lib
@@ -203,6 +204,31 @@ def hg_gather_fused(h: Handle, hidden: Sequence[torch.Tensor], weight: Sequence[
     st = load().hg_gather_fused(h.ptr, _ptr_array(hidden), _ptr_array(weight), lp,
                                 _ptr_array(outs), M, K, _stream_ptr(stream))
     _check(st, "hg_gather_fused")
+
+
+def new_row_stats(M: int, device="cuda") -> torch.Tensor:
+    """Device buffer for M hg_row_stats records (int32 [M, 4])."""
+    return torch.zeros((M, 4), dtype=torch.int32, device=device)
+
+
+def unpack_row_stats(stats: torch.Tensor) -> dict:
+    """max_logit, argmax, sum_exp, logsumexp columns of an hg_row_stats buffer."""
+    f = stats.view(torch.float32)
+    return {"max_logit": f[:, 0], "argmax": stats[:, 1], "sum_exp": f[:, 2], "logsumexp": f[:, 3]}
+
+
+def hg_gather_stats(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
+                    stats: torch.Tensor, M: int | None = None, stream=None) -> None:
+    """hg_gather plus per-row sampler statistics written into `stats`
+    (a buffer from new_row_stats(M))."""
+    M = shards[0].shape[0] if M is None else M
+    _check_tensors(shards, h.tp, h.shard_cols, M, "shards")
+    _check_tensors(outs, h.tp, h.V, M, "outs")
+    if not stats.is_cuda or stats.dtype != torch.int32 or tuple(stats.shape) != (M, 4) \
+            or not stats.is_contiguous():
+        raise ValueError("stats: need a contiguous int32 CUDA tensor [M, 4] (new_row_stats)")
+    _check(load().hg_gather_stats(h.ptr, _ptr_array(shards), _ptr_array(outs), M,
+                                  stats.data_ptr(), _stream_ptr(stream)), "hg_gather_stats")
 
 
 def hg_sync(h: Handle, stream=None) -> None:
