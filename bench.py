@@ -300,6 +300,38 @@ def workload_config(extra=None) -> dict:
     return c
 
 
+def graph_replay_us(torch, hg, synth, tp, W, cap, M, device, stream, calls, rows=None,
+                    seed=SEED, autotune=False, with_shape=False):
+    """us per call of `calls` gathers issued by replaying one CUDA graph of 200
+    captured calls (device-resident parity; no host work per call)."""
+    n = sets_for(tp, W, M)
+    h, sg, og_, cg = make_workload(torch, hg, synth, tp, W, cap, M, n, device, rows=rows,
+                                   seed=seed, device_parity=True, autotune=autotune)
+    cg[0]()
+    torch.cuda.synchronize()
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    n_graph = 200
+    with torch.cuda.stream(gs):
+        calls_g = [hg.GatherCall(h, [sg[i % n, r] for r in range(tp)],
+                                 [og_[i % n, d] for d in range(tp)], M, stream=gs)
+                   for i in range(n_graph)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for c in calls_g:
+            c()
+    torch.cuda.synchronize()
+    reps = max(1, calls // n_graph)
+    gms = time_calls(torch, [graph.replay], reps, 3, stream, "timed_graph")
+    hg.hg_sync(h)
+    us = round(gms * 1000.0 / (reps * n_graph), 3)
+    shape = hg.hg_launch_shape(h, M)
+    del graph
+    h.close()
+    del sg, og_, cg, calls_g
+    return (us, shape) if with_shape else us
+
+
 # --------------------------------------------------------------------- ours --
 
 def run_ours(args):
@@ -321,8 +353,10 @@ def run_ours(args):
     pk = peaks()
 
     # ---- step workload: config 2 ----
+    tune = args.autotune  # launch shapes timed on the device at hg_create
     nsets = sets_for(TP, W, M_STEP)
-    h, shards, outs, calls = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device)
+    h, shards, outs, calls = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device,
+                                           autotune=tune)
     shape = hg.hg_launch_shape(h, M_STEP)
     # correctness of the timed configuration, untimed: every set once
     for c in calls:
@@ -383,7 +417,7 @@ def run_ours(args):
         hg.hg_sync(h)
         torch_stats_us = round(t * 1000.0 / 200, 3)
         hdp, sdp, odp, cdp = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device,
-                                           device_parity=True)
+                                           device_parity=True, autotune=tune)
         t = time_calls(torch, cdp, args.steps, args.warmup, stream, "timed_devparity")
         hg.hg_sync(hdp)
         devpar_us = round(t * 1000.0 / args.steps, 3)
@@ -393,29 +427,8 @@ def run_ours(args):
     # ---- the same calls captured in a CUDA graph (device-resident parity) ----
     graph_us = None
     if not args.quick:
-        hgph, sg, og_, cg = make_workload(torch, hg, synth, TP, W, CAP, M_STEP, nsets, device,
-                                          device_parity=True)
-        cg[0]()
-        torch.cuda.synchronize()
-        gs = torch.cuda.Stream()
-        gs.wait_stream(torch.cuda.current_stream())
-        n_graph = 200
-        with torch.cuda.stream(gs):
-            calls_g = [hg.GatherCall(hgph, [sg[i % nsets, r] for r in range(TP)],
-                                     [og_[i % nsets, d] for d in range(TP)], M_STEP, stream=gs)
-                       for i in range(n_graph)]
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=gs):
-            for c in calls_g:
-                c()
-        torch.cuda.synchronize()
-        reps = max(1, args.steps // n_graph)
-        gms = time_calls(torch, [graph.replay], reps, 2, stream, "timed_graph")
-        hg.hg_sync(hgph)
-        graph_us = round(gms * 1000.0 / (reps * n_graph), 3)
-        del graph
-        hgph.close()
-        del sg, og_, cg
+        graph_us = graph_replay_us(torch, hg, synth, TP, W, CAP, M_STEP, device, stream,
+                                   args.steps, autotune=tune)
 
     # ---- e2e: pinned host buffers, H2D + gather + D2H per step ----
     host_in = [torch.empty((TP, M_STEP, W), dtype=torch.int16).pin_memory() for _ in range(3)]
@@ -445,20 +458,30 @@ def run_ours(args):
     del shards, outs, calls
 
     # ---- per-M (config 3 row counts) and large M ----
-    per_m = {}
+    per_m, per_m_shape, per_m_graph, per_m_graph_tuned, per_m_tuned_shape = {}, {}, {}, {}, {}
     if not args.quick:
         for M in range(1, 9):
             n = sets_for(TP, W, M)
-            hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, CAP, M, n, device, seed=2)
+            hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, CAP, M, n, device,
+                                              rows=[M], seed=2, autotune=tune)
             t = time_calls(torch, cm_, 200, 20, stream)
             hg.hg_sync(hm)
             per_m[str(M)] = round(t * 1000.0 / 200, 3)
+            per_m_shape[str(M)] = hg.hg_launch_shape(hm, M)
             hm.close()
             del sm_, om_, cm_
+            # host-free issue: 200 calls captured once, replayed (fixed rule, then
+            # shapes timed at hg_create)
+            per_m_graph[str(M)] = graph_replay_us(torch, hg, synth, TP, W, CAP, M, device,
+                                                  stream, 1000, rows=[M], seed=2)
+            per_m_graph_tuned[str(M)], per_m_tuned_shape[str(M)] = graph_replay_us(
+                torch, hg, synth, TP, W, CAP, M, device, stream, 1000, rows=[M], seed=2,
+                autotune=True, with_shape=True)
     large = {}
     for M in ([] if args.quick else [64, 128, 256]):
-        hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, M, M, 3, device, seed=3,
-                                          dist_kind="uniform", scale=20.0, sent=0.0)
+        hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, M, M, 3, device, rows=[M],
+                                          seed=3, dist_kind="uniform", scale=20.0, sent=0.0,
+                                          autotune=tune)
         reps = 30
         t = time_calls(torch, cm_, reps, 5, stream)
         hg.hg_sync(hm)
@@ -513,7 +536,8 @@ def run_ours(args):
             "l2": f"inputs+outputs rotate over {nsets} sets "
                   f"({nsets * TP * M_STEP * W * 2 * (1 + TP) / 2**20:.0f} MiB > 129 MB L2); "
                   "mailboxes (42 MB) are the method's persistent state",
-            "launch": dict(shape, launch="programmatic dependent launch")}),
+            "launch": dict(shape, launch="programmatic dependent launch",
+                           shapes="autotuned at hg_create" if tune else "fixed rule")}),
         "gpu_launches": args.steps,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
                 "h2d_bytes_per_step": TP * M_STEP * W * 2,
@@ -525,6 +549,10 @@ def run_ours(args):
                              f"{pk['source']} HBM copy bandwidth; at M=1 the working set is "
                              "L2-resident and the launch is latency-bound"},
         "per_m": per_m,
+        "per_m_launch": per_m_shape,
+        "per_m_graph_replay": per_m_graph,
+        "per_m_graph_replay_autotuned": per_m_graph_tuned,
+        "per_m_autotuned_launch": per_m_tuned_shape,
         "large_m": large,
         "with_row_stats_us_per_call": stats_us,
         "gather_then_torch_row_stats_us_per_call": torch_stats_us,
@@ -621,17 +649,19 @@ def run_sweep(args):
                 foot = n * M * tp * Wd * 2 * (1 + tp) + 2 * M * tp * tp * Wd * 2
                 if foot > args.max_gb * 2**30:
                     n = 2
-                h, s_, o_, c_ = make_workload(torch, hg, synth, tp, Wd, M, M, n, device, seed=3,
-                                              dist_kind="uniform", scale=20.0, sent=0.0,
-                                              elems_per_lane=args.vpt, ctas=args.ctas,
-                                              poll_mode=args.poll_mode,
-                                              cooperative=args.cooperative)
+                h, s_, o_, c_ = make_workload(torch, hg, synth, tp, Wd, M, M, n, device,
+                                              rows=[M], seed=3, dist_kind="uniform", scale=20.0,
+                                              sent=0.0, elems_per_lane=args.vpt, ctas=args.ctas,
+                                              prefetch=args.prefetch,
+                                              cooperative=args.cooperative,
+                                              autotune=args.autotune)
                 t = time_calls(torch, c_, args.calls, 10, stream)
                 hg.hg_sync(h)
                 us = t * 1000.0 / args.calls
                 gbs = algorithmic_bytes(tp, Wd, M) / (us * 1e-6) / 1e9
                 print(json.dumps({"sweep": "bandwidth", "tp": tp, "shard_cols": Wd, "M": M,
                                   "cooperative": args.cooperative,
+                                  "autotune": args.autotune,
                                   "cap": M, "calls": args.calls, "us_per_call": round(us, 3),
                                   "algorithmic_GBps": round(gbs, 1),
                                   "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 3),
@@ -680,7 +710,11 @@ def main(argv=None):
     ap.add_argument("--max-gb", type=float, default=120.0)
     ap.add_argument("--vpt", type=int, default=0, help="sweep: force elements per lane")
     ap.add_argument("--ctas", type=int, default=0, help="sweep: force the CTA count")
-    ap.add_argument("--poll-mode", type=int, default=0, help="sweep: 1 pipelined, 2 simple")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="sweep: 1 shard prefetch on, 2 off (0: chosen per row count)")
+    ap.add_argument("--autotune", action="store_true",
+                    help="launch shapes timed at hg_create (hg_options.autotune) instead of "
+                         "the library's fixed rule")
     ap.add_argument("--cooperative", action="store_true", help="sweep: cooperative launch")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -70,8 +70,9 @@ typedef struct hg_options {
   int ctas;                 /* CTAs of the gather kernel (32 * tp threads each);
                                default chosen per row count; clamped to what is
                                co-resident */
-  int poll_mode;            /* 0: by launch shape (pipelined when one wave
-                               covers the call), 1: pipelined, 2: simple */
+  int prefetch;             /* 0: chosen per row count (off unless tuned), 1: the
+                               next push's shard loads are issued one iteration
+                               ahead of its stores (overlapping a poll), 2: off */
   int cooperative;          /* 0 (default): programmatic dependent launch, the
                                next call's launch overlaps this one; 1:
                                cooperative launch, the runtime itself checks
@@ -83,6 +84,18 @@ typedef struct hg_options {
                                once every CTA has read it, so calls may be
                                captured into a CUDA graph and replayed; the
                                host learns the parity only at hg_sync */
+  int autotune;             /* 0 (default): launch shapes from a fixed rule; 1:
+                               hg_create_ex times candidate shapes (elements
+                               per lane, CTAs, prefetch) of every served row
+                               count on the device and keeps the fastest. The
+                               candidates honour the fields above that are
+                               set. The timed calls rotate over inputs and
+                               outputs in a zero-filled pool of max(256 MB,
+                               tp * M * (W + tp * W) * 2 bytes) that is freed
+                               before returning; row counts whose one set
+                               would exceed 1 GB keep the fixed rule. It costs
+                               tens of milliseconds per served row count at the
+                               decode sizes and changes no result, only speed */
 } hg_options;
 
 /*
@@ -161,10 +174,11 @@ int hg_parity(const hg_handle *h);
 int hg_mailbox(const hg_handle *h, int rank, const void **dev_ptr, size_t *bytes);
 
 /* Launch shape that hg_gather uses for row count M: CTAs, threads per CTA,
- * elements per lane and whether polls are pipelined (1) or simple (0). Any
- * output pointer may be NULL. Errors: HG_ERR_ARG, HG_ERR_ROWS. */
+ * elements per lane and whether the next push's shard loads are issued one
+ * iteration ahead (1) or not (0). Any output pointer may be NULL. Errors:
+ * HG_ERR_ARG, HG_ERR_ROWS. */
 int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *elems_per_lane,
-                    int *pipelined);
+                    int *prefetch);
 
 /*
  * Test hook for failure detection: make rank `rank`'s push skip its rows in

@@ -96,26 +96,92 @@ def test_parity_vs_oracle(tp, W, cap, Ms):
     run_sequence(tp, W, cap, Ms)
 
 
-@pytest.mark.parametrize("vpt,ctas,mode,coop", [
-    (1, 1, 0, False), (1, 3, 2, False), (2, 7, 0, False), (4, 2, 1, False), (2, 0, 1, False),
-    (4, 0, 2, False), (1, 0, 0, True), (4, 5, 2, True), (0, 0, 0, True)])
-def test_launch_shapes_vs_oracle(vpt, ctas, mode, coop):
+@pytest.mark.parametrize("vpt,ctas,pref,coop", [
+    (1, 1, 0, False), (1, 3, 1, False), (2, 7, 1, False), (4, 2, 2, False), (2, 0, 1, False),
+    (4, 0, 0, False), (1, 1, 1, False), (1, 0, 0, True), (4, 5, 1, True), (0, 0, 0, True)])
+def test_launch_shapes_vs_oracle(vpt, ctas, pref, coop):
     """Forced launch shapes: small grids make every CTA loop over many units (a
-    single CTA consumes its own pushes one iteration later); pipelined and
-    simple polls; cooperative and programmatic-dependent launches."""
-    run_sequence(4, 2048, 6, [6, 1, 5, 6], elems_per_lane=vpt, ctas=ctas, poll_mode=mode,
+    single CTA consumes its own pushes one iteration later); with and without
+    the shard prefetch; cooperative and programmatic-dependent launches."""
+    run_sequence(4, 2048, 6, [6, 1, 5, 6], elems_per_lane=vpt, ctas=ctas, prefetch=pref,
                  cooperative=coop)
+    h = hg.hg_create(4, 2048, 6, elems_per_lane=vpt, ctas=ctas, prefetch=pref)
+    assert hg.hg_launch_shape(h, 6)["prefetch"] == (pref == 1)
+    h.close()
 
 
 def test_multi_wave_decode_width_vs_oracle():
     """TP8, V=163840, M=64: more units than co-resident CTAs, so every CTA loops
-    over units with simple polls; three calls (both parities) against the
-    oracle word for word."""
+    over units; three calls (both parities) against the oracle word for word."""
     tp, W, M = 8, 20480, 64
     h = hg.hg_create(tp, W, M)
-    assert not hg.hg_launch_shape(h, M)["pipelined"]
+    shape = hg.hg_launch_shape(h, M)
+    units = M * tp * -(-(W // 8) // (32 * shape["elems_per_lane"]))
+    assert shape["ctas"] < units
     h.close()
     run_sequence(tp, W, M, [M, M, M])
+
+
+def _back_to_back(h, og, tp, W, Ms, seed):
+    """Issue every call of Ms on one stream with no synchronisation between
+    them (each into its own outputs), then compare all of them with the
+    oracle run through the same sequence."""
+    wants, outs_all = [], []
+    for i, M in enumerate(Ms):
+        bits = synth.shards(seed, tp, M, W, scale=3.0, sent_frac=0.01, set_index=i) \
+            .numpy().view(np.uint16)
+        wants.append(og.call(bits))
+        outs = empty_outs(tp, M, tp * W)
+        hg.hg_gather(h, to_dev(bits), outs, M)
+        outs_all.append(outs)
+    hg.hg_sync(h)
+    assert hg.hg_parity(h) == og.parity
+    for i, (want, outs) in enumerate(zip(wants, outs_all)):
+        got = from_dev(outs)
+        if not np.array_equal(got, want):
+            raise AssertionError(f"call {i} (M={Ms[i]}): {int((got != want).sum())} words differ")
+    assert_mailboxes_armed(h, hg)
+
+
+def test_varying_rows_back_to_back():
+    """TP8, V=163840: row counts 1, 1, 1, 2, 8, 3, 5, 4, 1, 8, 2 issued back to
+    back on one handle (each call's launch overlapping the previous one's
+    tail), synchronised only at the end; single-wave and looping grids
+    alternate from call to call."""
+    tp, W, cap = 8, 20480, 8
+    h = hg.hg_create(tp, W, cap)
+    og = oracle.Gather(tp, W, cap)
+    _back_to_back(h, og, tp, W, [1, 1, 1, 2, 8, 3, 5, 4, 1, 8, 2], seed=11)
+    h.close()
+
+
+def test_autotuned_shapes_vs_oracle():
+    """hg_options.autotune at the decode width (TP8, V=163840, the speculative
+    row counts): the tuned shapes are valid launch shapes, the parity starts at
+    0, and a seeded sequence of calls issued back to back matches the oracle;
+    the same with the parity on the device."""
+    tp, W, cap = 8, 20480, 8
+    rows = [1, 2, 3, 4, 5, 8]
+    for dp in (False, True):
+        h = hg.hg_create(tp, W, cap, rows, autotune=True, device_parity=dp)
+        assert hg.hg_parity(h) == 0
+        for M in rows:
+            s = hg.hg_launch_shape(h, M)
+            assert s["elems_per_lane"] in (1, 2, 4) and s["ctas"] >= 1
+            assert s["threads"] == 32 * tp
+        og = oracle.Gather(tp, W, cap, rows)
+        _back_to_back(h, og, tp, W, synth.row_sequence(5, 14, rows), seed=12 + dp)
+        h.close()
+
+
+def test_autotune_honours_forced_fields():
+    """Autotuning with elements per lane, CTAs and prefetch forced keeps them."""
+    h = hg.hg_create(4, 2048, 6, autotune=True, elems_per_lane=2, ctas=3, prefetch=1)
+    for M in range(1, 7):
+        s = hg.hg_launch_shape(h, M)
+        assert s["elems_per_lane"] == 2 and s["ctas"] == 3 and s["prefetch"]
+    h.close()
+    run_sequence(4, 2048, 6, [6, 1, 5], autotune=True)
 
 
 @pytest.mark.parametrize("tp", [24, 32])

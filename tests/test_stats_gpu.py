@@ -80,7 +80,7 @@ def test_stats_ties_and_special_rows():
 
 @pytest.mark.parametrize("tp,W,cap,Ms,kw", [
     (3, 6, 3, [3, 1], {}),                                 # word path (W % 8 != 0)
-    (4, 2048, 6, [6, 2], {"ctas": 3, "poll_mode": 2}),     # many units per CTA
+    (4, 2048, 6, [6, 2], {"ctas": 3, "prefetch": 1}),      # many units per CTA
     (16, 4096, 2, [2], {}),
     (8, 20480, 8, [8, 1], {"device_parity": True}),
     (1, 64, 2, [2, 1], {}),                                # degenerate TP=1

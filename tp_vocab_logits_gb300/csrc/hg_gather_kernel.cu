@@ -23,11 +23,12 @@
 // one-iteration lag keeps a pushed unit in L2 until it is polled and decouples
 // neighbouring CTAs.
 //
-// Polling. PIPE (single-wave launches, where the poll races the neighbour's
-// push): two staggered loads per waiting element stay in flight, so a word
-// that lands between two polls is seen about half an L2 round trip later
-// rather than a whole one. Otherwise (multi-iteration launches, where the data
-// was pushed an iteration earlier): load, check, re-load what is missing.
+// Polling: load every element of the unit, check, re-load only what still
+// holds a sentinel word; the loads land in the result registers directly.
+// PREF: the shard loads of the next push are issued one iteration ahead, so
+// that their latency overlaps this iteration's poll (multi-iteration
+// launches). Outputs are written with evict-first stores: the caller reads
+// them once, and L2 is better spent on the mailboxes.
 //
 // Memory ordering. Pushes, polls and re-arms are relaxed at gpu scope (morally
 // strong, per-word single-copy atomic; a vector access is one access per
@@ -43,16 +44,11 @@ namespace hg {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr unsigned kPollStaggerNs = 256;  // delay between the two in-flight polls
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
-}
-
-__device__ __forceinline__ void sleep_ns(unsigned ns) {
-  asm volatile("nanosleep.u32 %0;" :: "r"(ns));
 }
 
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
@@ -87,14 +83,9 @@ struct Elem<uint4> {
     asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
   }
-  template <bool STREAM>
   static __device__ __forceinline__ void st_out(uint4* p, uint4 v) {
-    if (STREAM)
-      asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
-                   :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-    else
-      asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
-                   :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
   }
   static __device__ __forceinline__ bool arrived(uint4 v) {
     return v.x != kSentinel && v.y != kSentinel && v.z != kSentinel && v.w != kSentinel;
@@ -128,12 +119,8 @@ struct Elem<uint32_t> {
   static __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
   }
-  template <bool STREAM>
   static __device__ __forceinline__ void st_out(uint32_t* p, uint32_t v) {
-    if (STREAM)
-      asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-    else
-      asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+    asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
   }
   static __device__ __forceinline__ bool arrived(uint32_t v) { return v != kSentinel; }
   static __device__ __forceinline__ uint32_t rewrite(uint32_t v) {
@@ -182,35 +169,11 @@ __device__ __forceinline__ void issue_polls(const V* box, const UnitPos& p, unsi
     if (todo >> v & 1) q[v] = Elem<V>::ld_poll(box + p.dst + 32 * v);
 }
 
-// Take the arrived elements of q into res; true when this warp is done. A lane
-// that waits too long (or sees an error raised elsewhere) gives up.
-template <typename V, int VPT>
-__device__ __forceinline__ bool take_arrived(const GatherArgs& a, const V (&q)[VPT],
-                                             V (&res)[VPT], unsigned& todo,
-                                             unsigned long long& t_wait, bool& gave_up, int u,
-                                             int d, size_t dst) {
-#pragma unroll
-  for (int v = 0; v < VPT; ++v)
-    if ((todo >> v & 1) && Elem<V>::arrived(q[v])) {
-      res[v] = q[v];
-      todo &= ~(1u << v);
-    }
-  if (todo) {
-    const unsigned long long now = globaltimer_ns();
-    if (t_wait == 0) t_wait = now;
-    if (now - t_wait > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
-      record_timeout(a, u, d, dst);
-      gave_up = true;
-      todo = 0;
-    }
-  }
-  return __all_sync(kFull, todo == 0);
-}
-
 // Poll this lane's elements of unit u in mailbox `box` until none holds a
-// sentinel word; res receives the data. The warp leaves together (vote).
-// Returns false when the warp gave up.
-template <typename V, int VPT, bool PIPE>
+// sentinel word; res receives the data. A lane that waits too long (or sees an
+// error raised elsewhere) gives up; the warp leaves together (vote). Returns
+// false when the warp gave up.
+template <typename V, int VPT>
 __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, const UnitPos& p,
                                           int u, int d, V (&res)[VPT]) {
   unsigned todo = 0;  // bit v: slot v still waits
@@ -219,24 +182,22 @@ __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, con
     if (p.idx + 32 * v < a.wv) todo |= 1u << v;
   unsigned long long t_wait = 0;
   bool gave_up = false;
-  V q0[VPT], q1[VPT];
+  issue_polls<V, VPT>(box, p, todo, res);
+  for (;;) {
 #pragma unroll
-  for (int v = 0; v < VPT; ++v) q0[v] = q1[v] = Elem<V>::sentinel();
-  issue_polls<V, VPT>(box, p, todo, q0);
-  if (PIPE) {
-    // Two loads in flight, issued a stagger apart; the loop is unrolled by two
-    // so that no register copy waits on a pending load.
-    for (;;) {
-      sleep_ns(kPollStaggerNs);
-      issue_polls<V, VPT>(box, p, todo, q1);
-      if (take_arrived<V, VPT>(a, q0, res, todo, t_wait, gave_up, u, d, p.dst)) break;
-      sleep_ns(kPollStaggerNs);
-      issue_polls<V, VPT>(box, p, todo, q0);
-      if (take_arrived<V, VPT>(a, q1, res, todo, t_wait, gave_up, u, d, p.dst)) break;
+    for (int v = 0; v < VPT; ++v)
+      if ((todo >> v & 1) && Elem<V>::arrived(res[v])) todo &= ~(1u << v);
+    if (todo) {
+      const unsigned long long now = globaltimer_ns();
+      if (t_wait == 0) t_wait = now;
+      if (now - t_wait > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+        record_timeout(a, u, d, p.dst);
+        gave_up = true;
+        todo = 0;
+      }
     }
-  } else {
-    while (!take_arrived<V, VPT>(a, q0, res, todo, t_wait, gave_up, u, d, p.dst))
-      issue_polls<V, VPT>(box, p, todo, q0);
+    if (__all_sync(kFull, todo == 0)) break;
+    issue_polls<V, VPT>(box, p, todo, res);
   }
   return !__any_sync(kFull, gave_up);
 }
@@ -385,12 +346,11 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a) {
   }
 }
 
-// VPT: elements per lane per unit. PIPE: staggered double polls (single-wave
-// launches). STREAM: evict-first stores of the outputs (multi-iteration
-// launches, whose outputs L2 should not keep). MAXT: largest CTA (32 * tp).
-// STATS: warp 0 (rank 0's copy of every row) also folds each consumed unit
-// into a statistics cell, and warp 0 of CTA 0 folds the cells of every row.
-template <typename V, int VPT, bool PIPE, bool STREAM, int MAXT, bool STATS>
+// VPT: elements per lane per unit. PREF: the next push's shard loads are
+// issued one iteration ahead. MAXT: largest CTA (32 * tp). STATS: warp 0
+// (rank 0's copy of every row) also folds each consumed unit into a
+// statistics cell, and warp 0 of CTA 0 folds the cells of every row.
+template <typename V, int VPT, bool PREF, int MAXT, bool STATS>
 __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
   // Programmatic dependent launch: wait until the previous kernel on the
@@ -442,30 +402,44 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
       if (p0.idx + 32 * v < a.wv) E::st_relaxed(box + p0.dst + 32 * v, E::rewrite(x0[v]));
   }
 
-  for (int t = 0; t <= iters; ++t) {
-    const int up = t * G + g;
-    if (t >= 1 && t < iters && up < N) {
-      const UnitPos p = unit_pos<VPT>(a, up, lane);
-      if (p.r != a.skip_rank) {
-        const V* src = reinterpret_cast<const V*>(a.shard[p.r]) + p.src;
-        V x[VPT];
-#pragma unroll
-        for (int v = 0; v < VPT; ++v)
-          if (p.idx + 32 * v < a.wv) x[v] = E::ld_shard(src + 32 * v);
-#pragma unroll
-        for (int v = 0; v < VPT; ++v)
-          if (p.idx + 32 * v < a.wv) E::st_relaxed(box + p.dst + 32 * v, E::rewrite(x[v]));
-      }
+  // Shard loads of a push: with PREF issued one iteration ahead (during the
+  // previous iteration's poll), otherwise right before the push's stores.
+  V xn[VPT];
+  UnitPos pn{};
+  bool pushn = false;
+  auto load_push = [&](int t) {
+    const int u = t * G + g;
+    pushn = t < iters && u < N;
+    if (!pushn) return;
+    pn = unit_pos<VPT>(a, u, lane);
+    if (pn.r == a.skip_rank) {
+      pushn = false;
+      return;
     }
+    const V* src = reinterpret_cast<const V*>(a.shard[pn.r]) + pn.src;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+      if (pn.idx + 32 * v < a.wv) xn[v] = E::ld_shard(src + 32 * v);
+  };
+  if (PREF) load_push(1);
+
+  for (int t = 1; t <= iters; ++t) {
+    if (!PREF) load_push(t);
+    if (pushn) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v)
+        if (pn.idx + 32 * v < a.wv) E::st_relaxed(box + pn.dst + 32 * v, E::rewrite(xn[v]));
+    }
+    if (PREF) load_push(t + 1);
     const int uc = (t - 1) * G + cons;
-    if (t >= 1 && uc < N) {
+    if (uc < N) {
       const UnitPos p = unit_pos<VPT>(a, uc, lane);
       V res[VPT];
-      if (!poll_unit<V, VPT, PIPE>(a, box, p, uc, d, res)) return;
+      if (!poll_unit<V, VPT>(a, box, p, uc, d, res)) return;
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
         if (p.idx + 32 * v < a.wv) {
-          E::template st_out<STREAM>(out + p.dst + 32 * v, res[v]);
+          E::st_out(out + p.dst + 32 * v, res[v]);
           E::st_relaxed(box + p.dst + 32 * v, E::sentinel());
         }
       }
@@ -496,32 +470,32 @@ __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
 // Kernels for tp <= 16 (CTAs of up to 512 threads) take 1, 2 or 4 elements
 // per lane; larger tp (up to 1024 threads, 64 registers) 1 or 2. Row
 // statistics exist for tp <= 16.
-template <typename V, bool PIPE, bool STATS>
+template <typename V, bool PREF, bool STATS>
 const void* pick_vpt(int vpt, int tp) {
   if (tp <= 16) {
     switch (vpt) {
-      case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 512, STATS>);
-      case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 512, STATS>);
-      case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4, PIPE, !PIPE, 512, STATS>);
+      case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PREF, 512, STATS>);
+      case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PREF, 512, STATS>);
+      case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4, PREF, 512, STATS>);
       default: return nullptr;
     }
   }
   if (STATS) return nullptr;
   switch (vpt) {
-    case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PIPE, !PIPE, 1024, false>);
-    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PIPE, !PIPE, 1024, false>);
+    case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PREF, 1024, false>);
+    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PREF, 1024, false>);
     default: return nullptr;
   }
 }
 
-template <typename V, bool PIPE>
+template <typename V, bool PREF>
 const void* pick_stats(const LaunchShape& s, int tp) {
-  return s.stats ? pick_vpt<V, PIPE, true>(s.vpt, tp) : pick_vpt<V, PIPE, false>(s.vpt, tp);
+  return s.stats ? pick_vpt<V, PREF, true>(s.vpt, tp) : pick_vpt<V, PREF, false>(s.vpt, tp);
 }
 
 const void* kernel_for(const LaunchShape& s, bool vec16, int tp) {
-  if (vec16) return s.pipe ? pick_stats<uint4, true>(s, tp) : pick_stats<uint4, false>(s, tp);
-  return s.pipe ? pick_stats<uint32_t, true>(s, tp) : pick_stats<uint32_t, false>(s, tp);
+  if (vec16) return s.pref ? pick_stats<uint4, true>(s, tp) : pick_stats<uint4, false>(s, tp);
+  return s.pref ? pick_stats<uint32_t, true>(s, tp) : pick_stats<uint32_t, false>(s, tp);
 }
 
 }  // namespace

@@ -63,11 +63,12 @@ struct GatherArgs {
 };
 
 // Launch shape of one row count: CTAs (32 * tp threads each), elements per lane
-// per unit, and the polling mode (pipelined for single-wave launches).
+// per unit, and whether the next push's shard loads are issued one iteration
+// ahead.
 struct LaunchShape {
   int ctas = 0;
   int vpt = 1;
-  bool pipe = true;
+  bool pref = false;
   bool stats = false;  // the kernel also folds row statistics
 };
 

@@ -61,47 +61,52 @@ void free_handle(hg_handle* h) {
   delete h;
 }
 
-// Launch shape for M rows. One CTA = one warp per virtual rank, each lane
-// carrying the widest unit (4 elements per lane; 2 for CTAs of 1024 threads):
-// measured at TP8, V=163840, fewer and fuller CTAs launch and finish sooner
-// (M=1: 160 CTAs 4.9 us/call against 640 CTAs 5.6 us/call). When every unit
-// fits in one wave of the pipelined-poll kernel, polls are pipelined (the poll
-// races the neighbour CTA's push); otherwise polls are simple and the grid is
-// the co-resident maximum of the simple kernel, looping over the units. The
+// Launch shape for M rows by a fixed rule. One CTA = one warp per virtual
+// rank, each lane carrying the widest unit (4 elements per lane; 2 for CTAs of
+// 1024 threads); one CTA per unit up to the co-resident maximum, beyond which
+// the CTAs loop over the units; no prefetch. Measured at TP8, V=163840 (us/
+// call, M = 1, 2, 3, 4, 8, 64): 3.6, 5.7, 6.0, 7.4, 11.4, 90.8. Other shapes
+// win at some row counts (M = 2: 2 elements per lane on 456 CTAs, 4.7 us), and
+// no simple rule finds them, so hg_options.autotune times the candidates. The
 // grid never exceeds the co-resident CTA count, which the kernel's cross-CTA
 // polls need.
+int max_vpt_of(const hg_handle* h) { return h->tp <= 16 ? 4 : 2; }  // 1024-thread CTAs stop at 2
+
+int check_shape_options(const hg_handle* h, const hg_options* opt) {
+  if (!opt) return HG_OK;
+  const int v = opt->elems_per_lane;
+  if (v != 0 && v != 1 && v != 2 && v != 4) return HG_ERR_ARG;
+  if (v > max_vpt_of(h) || opt->ctas < 0 || opt->prefetch < 0 || opt->prefetch > 2)
+    return HG_ERR_ARG;
+  if (opt->autotune < 0 || opt->autotune > 1) return HG_ERR_ARG;
+  return HG_OK;
+}
+
+// Co-resident CTAs of shape s on the whole device.
+int max_grid(const hg_handle* h, const hg::LaunchShape& s, long long* g) {
+  int per_sm = 0;
+  if (hg::gather_occupancy(s, h->vec16, h->tp, &per_sm) != cudaSuccess || per_sm < 1)
+    return HG_ERR_CUDA;
+  *g = (long long)per_sm * h->sms;
+  return HG_OK;
+}
+
 int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchShape* out,
              int* chunks_out) {
   const int forced_vpt = opt ? opt->elems_per_lane : 0;
   const int forced_ctas = opt ? opt->ctas : 0;
-  const int mode = opt ? opt->poll_mode : 0;
-  const int max_vpt = h->tp <= 16 ? 4 : 2;  // kernels of 1024-thread CTAs stop at 2
-  if (forced_vpt != 0 && forced_vpt != 1 && forced_vpt != 2 && forced_vpt != 4) return HG_ERR_ARG;
-  if (forced_vpt > max_vpt || forced_ctas < 0 || mode < 0 || mode > 2) return HG_ERR_ARG;
-  auto max_grid = [&](const hg::LaunchShape& s, long long* g) {
-    int per_sm = 0;
-    if (hg::gather_occupancy(s, h->vec16, h->tp, &per_sm) != cudaSuccess || per_sm < 1)
-      return HG_ERR_CUDA;
-    *g = (long long)per_sm * h->sms;
-    return HG_OK;
-  };
   hg::LaunchShape s;
   s.stats = stats;
-  s.vpt = forced_vpt ? forced_vpt : max_vpt;
+  s.vpt = forced_vpt ? forced_vpt : max_vpt_of(h);
+  s.pref = opt && opt->prefetch == 1;
   const int chunks = (h->wv + 32 * s.vpt - 1) / (32 * s.vpt);
   const long long units = (long long)M * h->tp * chunks;
   if (units > 0x7fffffffLL) return HG_ERR_ARG;
   long long want = forced_ctas ? forced_ctas : units;
   if (want > units) want = units;
   long long maxg = 0;
-  s.pipe = mode != 2;
-  int st = max_grid(s, &maxg);
+  const int st = max_grid(h, s, &maxg);
   if (st != HG_OK) return st;
-  if (mode == 0 && want > maxg) {  // more than one wave of the pipelined kernel
-    s.pipe = false;
-    st = max_grid(s, &maxg);
-    if (st != HG_OK) return st;
-  }
   long long G = want < maxg ? want : maxg;
   if (G < 1) G = 1;
   s.ctas = (int)G;
@@ -113,6 +118,8 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchS
 // Shapes of every served M, for hg_gather and (tp <= 16) hg_gather_stats, and
 // the number of statistics cells the largest stats call needs.
 int plan_shapes(hg_handle* h, const hg_options* opt) {
+  const int chk = check_shape_options(h, opt);
+  if (chk != HG_OK) return chk;
   h->shape.assign(h->cap + 1, hg::LaunchShape());
   h->chunks.assign(h->cap + 1, 0);
   h->shape_stats.assign(h->cap + 1, hg::LaunchShape());
@@ -135,6 +142,11 @@ int plan_shapes(hg_handle* h, const hg_options* opt) {
 }  // namespace
 
 extern "C" {
+
+namespace {
+// Defined below, next to gather_impl, whose calls it times.
+int autotune_shapes(hg_handle* h, const hg_options* opt);
+}  // namespace
 
 const char* hg_strerror(int status) {
   switch (status) {
@@ -214,6 +226,16 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
       return HG_ERR_CUDA;
     }
   }
+  if (cudaMalloc(&h->status, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
+      cudaMemset(h->status, 0, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    free_handle(h);
+    return HG_ERR_CUDA;
+  }
+  if (opt && opt->autotune) {
+    st = autotune_shapes(h, opt);
+    if (st != HG_OK) { free_handle(h); return st; }
+  }
   if (h->device_parity) {
     // One copy per reader: warp d of CTA g of a gather reads copy g * tp + d,
     // CTA g of a fused call (at most one CTA per SM) reads copy g.
@@ -224,16 +246,11 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
     }
     h->parity_entries = max_ctas * tp > h->sms ? max_ctas * tp : h->sms;
     if (cudaMalloc(&h->parity_words, (size_t)h->parity_entries * sizeof(int)) != cudaSuccess ||
-        cudaMemset(h->parity_words, 0, (size_t)h->parity_entries * sizeof(int)) != cudaSuccess) {
+        cudaMemset(h->parity_words, 0, (size_t)h->parity_entries * sizeof(int)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
       free_handle(h);
       return HG_ERR_CUDA;
     }
-  }
-  if (cudaMalloc(&h->status, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
-      cudaMemset(h->status, 0, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess) {
-    free_handle(h);
-    return HG_ERR_CUDA;
   }
   *out = h;
   return HG_OK;
@@ -306,6 +323,167 @@ int gather_impl(hg_handle* h, const void* const* shard_ptrs, void* const* out_pt
   return HG_OK;
 }
 
+// One candidate launch shape of the autotuner.
+struct Candidate {
+  hg::LaunchShape s;
+  int chunks = 0;
+  float us = 1e30f;
+};
+
+// Candidate shapes of row count M: every allowed (elements per lane,
+// prefetch) pair, each on one CTA per unit (capped at the co-resident
+// maximum) and on k CTAs per SM for every k below the co-resident count
+// that leaves CTAs looping over units. Prefetch only with two or more
+// iterations (otherwise it is the same kernel work as without).
+int tune_candidates(hg_handle* h, int M, const hg_options* opt, std::vector<Candidate>* out) {
+  std::vector<int> vpts;
+  if (opt->elems_per_lane) vpts.push_back(opt->elems_per_lane);
+  else for (int v = 1; v <= max_vpt_of(h); v *= 2) vpts.push_back(v);
+  std::vector<bool> prefs;
+  if (opt->prefetch == 0 || opt->prefetch == 2) prefs.push_back(false);
+  if (opt->prefetch == 0 || opt->prefetch == 1) prefs.push_back(true);
+  for (int vpt : vpts) {
+    for (bool pref : prefs) {
+      Candidate c;
+      c.s.vpt = vpt;
+      c.s.pref = pref;
+      c.chunks = (h->wv + 32 * vpt - 1) / (32 * vpt);
+      const long long units = (long long)M * h->tp * c.chunks;
+      if (units > 0x7fffffffLL) continue;
+      long long maxg = 0;
+      const int st = max_grid(h, c.s, &maxg);
+      if (st != HG_OK) return st;
+      std::vector<long long> grids;
+      if (opt->ctas) {
+        long long g = opt->ctas < units ? opt->ctas : units;
+        grids.push_back(g < maxg ? g : maxg);
+      } else {
+        grids.push_back(units < maxg ? units : maxg);
+        for (long long g = h->sms; g < maxg && g < units; g += h->sms) grids.push_back(g);
+      }
+      for (long long g : grids) {
+        const long long iters = (units + g - 1) / g;
+        if (pref && iters < 2) continue;
+        c.s.ctas = (int)g;
+        out->push_back(c);
+      }
+    }
+  }
+  return HG_OK;
+}
+
+// hg_options.autotune: time the candidate shapes of every served row count
+// (whose inputs and outputs, one set, stay within kSetLimit) and keep the
+// fastest. Timing: calls back to back on a private stream, as a decode loop
+// issues them, rotating over as many sets of inputs and outputs as fit in a
+// zero-filled pool of at least kPoolBytes (more than twice the L2), so that
+// they stream from HBM as in a long run of calls. Each measurement is 2 calls
+// of warm-up, then a block of calls timed with events, sized to about
+// kBlockUs of device time (4 to 32 calls); three rounds over all candidates,
+// interleaved so that a slow stretch of the device does not fall on one
+// candidate alone, the fastest block of each candidate kept. The calls gather
+// real data through the handle's mailboxes, which every call leaves armed;
+// the parity is reset to 0 afterwards.
+int autotune_shapes(hg_handle* h, const hg_options* opt) {
+  constexpr size_t kSetLimit = 1ull << 30;
+  constexpr size_t kPoolBytes = 256ull << 20;
+  constexpr float kBlockUs = 300.f;
+  constexpr int kRounds = 3;
+  const size_t V = (size_t)h->tp * h->W;
+  // One set: tp shards [M][W], then tp outputs [M][V], each 16-byte aligned.
+  auto set_bytes = [&](int M) { return (size_t)h->tp * M * (h->W + V) * 2; };
+  int maxM = 0;
+  for (int M = 1; M <= h->cap; ++M)
+    if (h->served[M] && set_bytes(M) <= kSetLimit) maxM = M;
+  if (maxM == 0) return HG_OK;
+  const size_t pool_bytes = set_bytes(maxM) > kPoolBytes ? set_bytes(maxM) : kPoolBytes;
+  char* pool = nullptr;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  const bool saved_dp = h->device_parity;
+  h->device_parity = false;  // host parity while tuning: parity copies do not exist yet
+  int rc = HG_OK;
+  if (cudaMalloc(&pool, pool_bytes) != cudaSuccess || cudaMemset(pool, 0, pool_bytes) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    rc = HG_ERR_CUDA;
+  std::vector<const void*> shard(h->tp);
+  std::vector<void*> out(h->tp);
+  int call = 0;
+  auto run = [&](int M, const Candidate& c, int calls) {
+    h->shape[M] = c.s;
+    h->chunks[M] = c.chunks;
+    const size_t sb = set_bytes(M);
+    const int sets = (int)(pool_bytes / sb);
+    for (int i = 0; i < calls; ++i, ++call) {
+      char* base = pool + (size_t)(call % sets) * sb;
+      for (int r = 0; r < h->tp; ++r) {
+        shard[r] = base + (size_t)r * M * h->W * 2;
+        out[r] = base + (size_t)h->tp * M * h->W * 2 + (size_t)r * M * V * 2;
+      }
+      const int st = gather_impl(h, shard.data(), out.data(), M, nullptr, stream);
+      if (st != HG_OK) return st;
+    }
+    return (int)HG_OK;
+  };
+  for (int M = 1; M <= maxM && rc == HG_OK; ++M) {
+    if (!h->served[M]) continue;
+    std::vector<Candidate> cand;
+    rc = tune_candidates(h, M, opt, &cand);
+    if (rc != HG_OK || cand.empty()) break;
+    // Time `calls` calls of candidate c (after 2 of warm-up), in us per call.
+    auto timed = [&](const Candidate& c, int calls, float* us) {
+      int st = run(M, c, 2);
+      if (st != HG_OK) return st;
+      if (cudaEventRecord(e0, stream) != cudaSuccess) return (int)HG_ERR_CUDA;
+      st = run(M, c, calls);
+      if (st != HG_OK) return st;
+      float ms = 0.f;
+      if (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+        return (int)HG_ERR_CUDA;
+      *us = ms * 1000.f / calls;
+      return (int)HG_OK;
+    };
+    if (call == 0) rc = run(M, cand[0], 200);  // clocks up before the first timing
+    float est = 0.f;
+    if (rc == HG_OK) rc = timed(cand[0], 8, &est);  // block size from the first candidate
+    int block = est > 0.f ? (int)(kBlockUs / est) : 32;
+    block = block < 4 ? 4 : (block > 32 ? 32 : block);
+    for (int round = 0; round < kRounds && rc == HG_OK; ++round) {
+      for (Candidate& c : cand) {
+        float us = 0.f;
+        rc = timed(c, block, &us);
+        if (rc != HG_OK) break;
+        if (us < c.us) c.us = us;
+      }
+    }
+    if (rc != HG_OK) break;
+    const Candidate* best = &cand[0];
+    for (const Candidate& c : cand)
+      if (c.us < best->us) best = &c;
+    h->shape[M] = best->s;
+    h->chunks[M] = best->chunks;
+  }
+  if (stream) {
+    int status = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess ||
+        cudaMemcpy(&status, h->status, sizeof status, cudaMemcpyDeviceToHost) != cudaSuccess) {
+      if (rc == HG_OK) rc = HG_ERR_CUDA;
+    } else if (status != hg::kDevOk && rc == HG_OK) {
+      rc = HG_ERR_TIMEOUT;
+    }
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (stream) cudaStreamDestroy(stream);
+  if (pool) cudaFree(pool);
+  h->device_parity = saved_dp;
+  h->parity = 0;
+  return rc;
+}
+
 }  // namespace
 
 int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
@@ -365,14 +543,14 @@ int hg_mailbox(const hg_handle* h, int rank, const void** dev_ptr, size_t* bytes
 }
 
 int hg_launch_shape(const hg_handle* h, int M, int* ctas, int* threads, int* elems_per_lane,
-                    int* pipelined) {
+                    int* prefetch) {
   if (!h) return HG_ERR_ARG;
   if (M < 1 || M > h->cap || !h->served[M]) return HG_ERR_ROWS;
   const hg::LaunchShape& s = h->shape[M];
   if (ctas) *ctas = s.ctas;
   if (threads) *threads = 32 * h->tp;
   if (elems_per_lane) *elems_per_lane = s.vpt;
-  if (pipelined) *pipelined = s.pipe ? 1 : 0;
+  if (prefetch) *prefetch = s.pref ? 1 : 0;
   return HG_OK;
 }
 

@@ -111,22 +111,15 @@ extern "C" int hg_gather_static(int tp, int shard_cols, const void* const* shard
   a.M = M;
   a.skip_rank = -1;
 
-  // Launch shape: widest unit; pipelined polls when one wave of that kernel
-  // covers every unit, else simple polls over the co-resident grid.
+  // Launch shape: widest unit, one CTA per unit up to the co-resident
+  // maximum (beyond it the CTAs loop over the units).
   hg::LaunchShape s;
   s.vpt = tp <= 16 ? 4 : 2;
   a.chunks = (wv + 32 * s.vpt - 1) / (32 * s.vpt);
   const long long units = (long long)M * tp * a.chunks;
   int per_sm = 0;
-  s.pipe = true;
   if (hg::gather_occupancy(s, vec16, tp, &per_sm) != cudaSuccess || per_sm < 1) return HG_ERR_CUDA;
-  long long maxg = (long long)per_sm * ds.sms;
-  if (units > maxg) {
-    s.pipe = false;
-    if (hg::gather_occupancy(s, vec16, tp, &per_sm) != cudaSuccess || per_sm < 1)
-      return HG_ERR_CUDA;
-    maxg = (long long)per_sm * ds.sms;
-  }
+  const long long maxg = (long long)per_sm * ds.sms;
   s.ctas = (int)(units < maxg ? units : maxg);
 
   // The array keeps the last call's contents: clear the status words and arm

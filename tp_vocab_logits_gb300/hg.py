@@ -29,8 +29,8 @@ class HGError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("poll_timeout_ns", ctypes.c_uint64), ("elems_per_lane", ctypes.c_int),
-                ("ctas", ctypes.c_int), ("poll_mode", ctypes.c_int), ("cooperative", ctypes.c_int),
-                ("device_parity", ctypes.c_int)]
+                ("ctas", ctypes.c_int), ("prefetch", ctypes.c_int), ("cooperative", ctypes.c_int),
+                ("device_parity", ctypes.c_int), ("autotune", ctypes.c_int)]
 
 
 _LIB: ctypes.CDLL | None = None
@@ -123,15 +123,16 @@ class Handle:
 
 def hg_create(tp: int, shard_cols: int, cap: int, rows: Sequence[int] | None = None, *,
               poll_timeout_ns: int = 0, elems_per_lane: int = 0, ctas: int = 0,
-              poll_mode: int = 0, cooperative: bool = False,
-              device_parity: bool = False) -> Handle:
+              prefetch: int = 0, cooperative: bool = False,
+              device_parity: bool = False, autotune: bool = False) -> Handle:
     lib = load()
     rows = list(rows or [])
     arr = (ctypes.c_int * max(1, len(rows)))(*rows)
     out = ctypes.c_void_p()
-    if poll_timeout_ns or elems_per_lane or ctas or poll_mode or cooperative or device_parity:
-        opt = _Options(poll_timeout_ns, elems_per_lane, ctas, poll_mode, int(bool(cooperative)),
-                       int(bool(device_parity)))
+    if poll_timeout_ns or elems_per_lane or ctas or prefetch or cooperative or device_parity \
+            or autotune:
+        opt = _Options(poll_timeout_ns, elems_per_lane, ctas, prefetch, int(bool(cooperative)),
+                       int(bool(device_parity)), int(bool(autotune)))
         st = lib.hg_create_ex(tp, shard_cols, cap, arr, len(rows), ctypes.byref(opt),
                               ctypes.byref(out))
     else:
@@ -270,12 +271,12 @@ def mailbox_words(h: Handle, rank: int) -> torch.Tensor:
 
 
 def hg_launch_shape(h: Handle, M: int) -> dict:
-    """Launch shape of row count M: ctas, threads, elems_per_lane, pipelined."""
+    """Launch shape of row count M: ctas, threads, elems_per_lane, prefetch."""
     c, t, e, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     _check(load().hg_launch_shape(h.ptr, M, ctypes.byref(c), ctypes.byref(t), ctypes.byref(e),
                                   ctypes.byref(p)), "hg_launch_shape")
     return {"ctas": c.value, "threads": t.value, "elems_per_lane": e.value,
-            "pipelined": bool(p.value)}
+            "prefetch": bool(p.value)}
 
 
 def hg_debug_skip_push(h: Handle, rank: int) -> None:
