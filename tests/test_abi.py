@@ -61,3 +61,29 @@ def test_host_checks_without_device(lib):
     for code in range(7):
         assert lib.hg_strerror(code)
     assert lib.hg_strerror(99) == b"unknown status"
+
+
+def test_direct_call_object_marshals_and_raises(lib):
+    """The _hgcall extension builds and loads, holds the pointer lists, calls
+    the C entry point and turns a failed status into HGError: here a closed
+    handle (NULL), which hg_gather rejects before any CUDA call."""
+    mod = hg._pycall()
+
+    class Closed:
+        ptr = None
+
+    fn = ctypes.cast(lib.hg_gather, ctypes.c_void_p).value
+    raised = []
+
+    def on_error(status):
+        raised.append(status)
+        raise hg.HGError(status, "hg_gather")
+
+    call = mod.Call(fn, Closed(), [16, 32], [48, 64], 1, 0, None, on_error)
+    with pytest.raises(hg.HGError):
+        call()
+    assert raised == [hg.HG_ERR_ARG]
+    with pytest.raises(TypeError):
+        call(1)
+    with pytest.raises(ValueError):
+        mod.Call(fn, Closed(), [16, 32], [48], 1, 0, None, on_error)

@@ -4,6 +4,9 @@ Each .cu file under csrc/ is compiled by nvcc in parallel, then linked into
 tp_vocab_logits_gb300/libhg.so (static CUDA runtime, so the library needs
 nothing beyond the driver at run time). ptxas resource usage (registers,
 spills, shared memory) of the last build is kept in _build/ptxas.log.
+
+Alongside, csrc/hg_pycall.c is compiled with the host C compiler into the
+CPython extension _hgcall (the Python binding's direct-call object).
 """
 
 from __future__ import annotations
@@ -13,6 +16,7 @@ import os
 import shutil
 import subprocess
 import sys
+import sysconfig
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -20,6 +24,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhg.so")
+PYCALL_SRC = os.path.join(CSRC, "hg_pycall.c")
+PYCALL = os.path.join(PKG, "_hgcall" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
@@ -42,10 +48,20 @@ def _deps() -> list:
 
 
 def stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(PYCALL):
         return True
-    t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(p) > t for p in _deps() + [__file__])
+    t = min(os.path.getmtime(LIB), os.path.getmtime(PYCALL))
+    return any(os.path.getmtime(p) > t for p in _deps() + [PYCALL_SRC, __file__])
+
+
+def _pycall_cmd(out: str) -> list:
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        raise RuntimeError("a C compiler (gcc) is required to build the _hgcall extension")
+    inc = sysconfig.get_paths()["include"]
+    if not os.path.exists(os.path.join(inc, "Python.h")):
+        raise RuntimeError(f"Python.h not found under {inc}: the _hgcall extension needs it")
+    return [cc, "-O2", "-shared", "-fPIC", "-Wall", f"-I{inc}", PYCALL_SRC, "-o", out]
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -56,6 +72,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     exe = nvcc()
     procs = []
     objs = []
+    pycall_tmp = PYCALL + f".{os.getpid()}.tmp"
+    procs.append((PYCALL_SRC, subprocess.Popen(_pycall_cmd(pycall_tmp), stdout=subprocess.PIPE,
+                                               stderr=subprocess.STDOUT, text=True)))
     for src in sources():
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
@@ -77,6 +96,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     tmp = LIB + f".{os.getpid()}.tmp"
     subprocess.run([exe, *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB)
+    os.replace(pycall_tmp, PYCALL)
     if verbose:
         print("\n".join(logs))
     return LIB

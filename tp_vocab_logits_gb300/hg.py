@@ -157,25 +157,37 @@ def _check_tensors(ts: Sequence[torch.Tensor], n: int, cols: int, M: int, what: 
             raise ValueError(f"{what}: need contiguous [{M}, {cols}], got {tuple(t.shape)}")
 
 
-class GatherCall:
+def GatherCall(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor], M: int,
+               stream=None):
     """Marshalled arguments of one hg_gather call, reusable across calls with
-    the same buffers (keeps per-call host work to the C call itself)."""
+    the same buffers: returns a callable that makes the call (raising HGError
+    on a failed status). The callable is a small CPython object (the _hgcall
+    extension) that calls the C entry point directly, so per-call host work
+    is the C call itself."""
+    _check_tensors(shards, h.tp, h.shard_cols, M, "shards")
+    _check_tensors(outs, h.tp, h.V, M, "outs")
+    fn = ctypes.cast(load().hg_gather, ctypes.c_void_p).value
+    return _pycall().Call(fn, h, [t.data_ptr() for t in shards], [t.data_ptr() for t in outs],
+                          M, _stream_ptr(stream), (list(shards), list(outs)), _raise_gather)
 
-    def __init__(self, h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
-                 M: int, stream=None):
-        _check_tensors(shards, h.tp, h.shard_cols, M, "shards")
-        _check_tensors(outs, h.tp, h.V, M, "outs")
-        self.h, self.M = h, M
-        self._keep = (list(shards), list(outs))
-        self._sp = _ptr_array(shards)
-        self._op = _ptr_array(outs)
-        self._stream = _stream_ptr(stream)
-        self._fn = load().hg_gather
 
-    def __call__(self) -> None:
-        st = self._fn(self.h.ptr, self._sp, self._op, self.M, self._stream)
-        if st != HG_OK:
-            raise HGError(st, "hg_gather")
+def _raise_gather(status: int) -> None:
+    raise HGError(status, "hg_gather")
+
+
+_PYCALL = None
+
+
+def _pycall():
+    """The _hgcall extension (built in-tree next to libhg.so); raises if absent."""
+    global _PYCALL
+    if _PYCALL is None:
+        import importlib
+        if not os.path.exists(_build.PYCALL):
+            raise RuntimeError(f"{_build.PYCALL} is missing: build it with "
+                               "tp_vocab_logits_gb300._build.build()")
+        _PYCALL = importlib.import_module("tp_vocab_logits_gb300._hgcall")
+    return _PYCALL
 
 
 def hg_gather(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
