@@ -153,6 +153,26 @@ int hg_destroy(hg_handle *h);
 int hg_gather(hg_handle *h, const void *const *shard_ptrs, void *const *out_ptrs, int M,
               hg_stream_t stream);
 
+/*
+ * hg_gather_host - hg_gather whose shards and outputs may live in page-locked
+ * host memory (cudaHostAlloc, cudaMallocHost or cudaHostRegister), as well as
+ * in device memory of the handle's device. The pages define the gather on
+ * device buffers only; this entry point is this library's end-to-end form for
+ * a host that holds the logits: the same kernel reads the shards from host
+ * memory and writes the outputs into host memory directly over the
+ * host-device link (no staging copies), while the mailboxes stay in device
+ * memory. Same arguments, contract and errors as hg_gather, plus:
+ *
+ *   every pointer is checked with cudaPointerGetAttributes and replaced by its
+ *   device-side address; pageable host memory, memory of another device and
+ *   unknown addresses give HG_ERR_ARG before any device work.
+ *
+ * The outputs are complete in host memory once the stream has passed the
+ * call (e.g. after hg_sync or a stream synchronisation).
+ */
+int hg_gather_host(hg_handle *h, const void *const *shard_ptrs, void *const *out_ptrs, int M,
+                   hg_stream_t stream);
+
 /* Wait for `stream`, then read the device status word. Returns HG_OK,
  * HG_ERR_TIMEOUT (a poll gave up; mailbox contents undefined until hg_rearm)
  * or HG_ERR_CUDA. */

@@ -50,6 +50,7 @@ def test_host_checks_without_device(lib):
     assert lib.hg_create(2, 64, 4, rows, 2, ctypes.byref(out)) == hg.HG_ERR_ARG
     assert lib.hg_create(2, 64, 4, None, 0, None) == hg.HG_ERR_ARG
     assert lib.hg_gather(None, None, None, 1, None) == hg.HG_ERR_ARG
+    assert lib.hg_gather_host(None, None, None, 1, None) == hg.HG_ERR_ARG
     assert lib.hg_sync(None, None) == hg.HG_ERR_ARG
     assert lib.hg_rearm(None, None) == hg.HG_ERR_ARG
     assert lib.hg_parity(None) == -1

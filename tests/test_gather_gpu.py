@@ -267,6 +267,52 @@ def test_config4_large_points_properties(tp, W, M):
     h.close()
 
 
+@pytest.mark.parametrize("shards_on_host", [True, False])
+def test_host_buffers_vs_oracle(shards_on_host):
+    """hg_gather_host at the decode width (TP8, V=163840): outputs in
+    page-locked host memory written by the kernel itself, shards in host or
+    device memory; every call against the oracle, both parities, rows 1..3."""
+    tp, W, cap = 8, 20480, 4
+    h = hg.hg_create(tp, W, cap)
+    og = oracle.Gather(tp, W, cap)
+    for i, M in enumerate([1, 3, 2, 1]):
+        bits = synth.shards(21, tp, M, W, scale=3.0, sent_frac=0.01, set_index=i) \
+            .numpy().view(np.uint16)
+        want = og.call(bits)
+        host_sh = [torch.from_numpy(bits[r].view(np.int16).copy()).pin_memory()
+                   for r in range(tp)]
+        shards = host_sh if shards_on_host else [t.cuda() for t in host_sh]
+        outs = [torch.full((M, tp * W), 7, dtype=torch.int16).pin_memory() for _ in range(tp)]
+        hg.hg_gather_host(h, shards, outs, M)
+        hg.hg_sync(h)
+        got = np.stack([o.numpy().view(np.uint16) for o in outs])
+        np.testing.assert_array_equal(got, want)
+        assert hg.hg_parity(h) == og.parity
+    assert_mailboxes_armed(h, hg)
+    h.close()
+
+
+def test_host_buffers_rejects_pageable_memory():
+    """Pageable host memory (not page-locked) is refused before any device
+    work, with no parity flip; the binding refuses it before the call."""
+    import ctypes
+    tp, W = 2, 64
+    h = hg.hg_create(tp, W, 2)
+    lib = hg.load()
+    pageable = [np.zeros((1, W), np.int16) for _ in range(tp)]
+    outs_p = [np.zeros((1, tp * W), np.int16) for _ in range(tp)]
+    sp = (ctypes.c_void_p * tp)(*[a.ctypes.data for a in pageable])
+    op = (ctypes.c_void_p * tp)(*[a.ctypes.data for a in outs_p])
+    assert lib.hg_gather_host(h.ptr, sp, op, 1, None) == hg.HG_ERR_ARG
+    assert hg.hg_parity(h) == 0
+    with pytest.raises(ValueError):
+        hg.hg_gather_host(h, [torch.zeros(1, W, dtype=torch.int16) for _ in range(tp)],
+                          [torch.zeros(1, tp * W, dtype=torch.int16).pin_memory()
+                           for _ in range(tp)], 1)
+    hg.hg_sync(h)
+    h.close()
+
+
 def test_stock_baseline_matches_concat():
     """The cudaMemcpy2D baseline is the plain concat; without sentinel words it
     equals the gather bit for bit."""

@@ -491,6 +491,45 @@ int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs
   return gather_impl(h, shard_ptrs, out_ptrs, M, nullptr, stream);
 }
 
+namespace {
+
+// Device-side address of p, which must be page-locked host memory or device
+// memory of device `dev` (HG_ERR_ARG otherwise).
+int device_view(const void* p, int dev, void** out) {
+  if (!p) return HG_ERR_ARG;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return HG_ERR_ARG;
+  }
+  if (!at.devicePointer) return HG_ERR_ARG;
+  if (at.type == cudaMemoryTypeHost) {
+    *out = at.devicePointer;
+    return HG_OK;
+  }
+  if ((at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev) {
+    *out = at.devicePointer;
+    return HG_OK;
+  }
+  return HG_ERR_ARG;  // pageable host memory or another device's memory
+}
+
+}  // namespace
+
+int hg_gather_host(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
+                   hg_stream_t stream) {
+  if (!h || !shard_ptrs || !out_ptrs) return HG_ERR_ARG;
+  const void* sh[HG_MAX_TP];
+  void* ou[HG_MAX_TP];
+  for (int r = 0; r < h->tp; ++r) {
+    void* p = nullptr;
+    if (device_view(shard_ptrs[r], h->device, &p) != HG_OK) return HG_ERR_ARG;
+    sh[r] = p;
+    if (device_view(out_ptrs[r], h->device, &ou[r]) != HG_OK) return HG_ERR_ARG;
+  }
+  return gather_impl(h, sh, ou, M, nullptr, stream);
+}
+
 int hg_gather_stats(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
                     hg_row_stats* stats, hg_stream_t stream) {
   if (!stats) return HG_ERR_ARG;

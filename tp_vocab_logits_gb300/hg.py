@@ -55,6 +55,7 @@ def load() -> ctypes.CDLL:
                                  ctypes.POINTER(vp)]
     lib.hg_destroy.argtypes = [vp]
     lib.hg_gather.argtypes = [vp, vpp, vpp, i, st]
+    lib.hg_gather_host.argtypes = [vp, vpp, vpp, i, st]
     lib.hg_sync.argtypes = [vp, st]
     lib.hg_rearm.argtypes = [vp, st]
     lib.hg_parity.argtypes = [vp]
@@ -67,7 +68,8 @@ def load() -> ctypes.CDLL:
     lib.hg_gather_stats.argtypes = [vp, vpp, vpp, i, vp, st]
     lib.hg_strerror.argtypes = [i]
     lib.hg_strerror.restype = ctypes.c_char_p
-    for name in ("hg_create", "hg_create_ex", "hg_destroy", "hg_gather", "hg_sync", "hg_rearm",
+    for name in ("hg_create", "hg_create_ex", "hg_destroy", "hg_gather", "hg_gather_host",
+                 "hg_sync", "hg_rearm",
                  "hg_parity", "hg_mailbox", "hg_launch_shape", "hg_debug_skip_push",
                  "hg_stock_gather", "hg_gather_fused", "hg_gather_stats"):
         getattr(lib, name).restype = i
@@ -145,11 +147,15 @@ def hg_destroy(h: Handle) -> None:
     h.close()
 
 
-def _check_tensors(ts: Sequence[torch.Tensor], n: int, cols: int, M: int, what: str) -> None:
+def _check_tensors(ts: Sequence[torch.Tensor], n: int, cols: int, M: int, what: str,
+                   host: bool = False) -> None:
     if len(ts) != n:
         raise ValueError(f"{what}: expected {n} tensors, got {len(ts)}")
     for t in ts:
-        if not t.is_cuda:
+        if host:
+            if not t.is_cuda and not t.is_pinned():
+                raise ValueError(f"{what}: host tensors must be in page-locked memory")
+        elif not t.is_cuda:
             raise ValueError(f"{what}: tensors must be on a CUDA device")
         if t.dtype not in (torch.bfloat16, torch.int16):
             raise ValueError(f"{what}: dtype must be bfloat16 (or its int16 bits), got {t.dtype}")
@@ -163,10 +169,14 @@ def GatherCall(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.T
     the same buffers: returns a callable that makes the call (raising HGError
     on a failed status). The callable is a small CPython object (the _hgcall
     extension) that calls the C entry point directly, so per-call host work
-    is the C call itself."""
-    _check_tensors(shards, h.tp, h.shard_cols, M, "shards")
-    _check_tensors(outs, h.tp, h.V, M, "outs")
-    fn = ctypes.cast(load().hg_gather, ctypes.c_void_p).value
+    is the C call itself. When any tensor is in (page-locked) host memory the
+    call is hg_gather_host: the kernel reads and writes host memory directly
+    over the host-device link."""
+    host = any(not t.is_cuda for t in list(shards) + list(outs))
+    _check_tensors(shards, h.tp, h.shard_cols, M, "shards", host)
+    _check_tensors(outs, h.tp, h.V, M, "outs", host)
+    entry = load().hg_gather_host if host else load().hg_gather
+    fn = ctypes.cast(entry, ctypes.c_void_p).value
     return _pycall().Call(fn, h, [t.data_ptr() for t in shards], [t.data_ptr() for t in outs],
                           M, _stream_ptr(stream), (list(shards), list(outs)), _raise_gather)
 
@@ -194,6 +204,15 @@ def hg_gather(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Te
               M: int | None = None, stream=None) -> None:
     """One gather: shards[r] is rank r's [M, W] bf16 logits, outs[d] rank d's
     [M, V] bf16 output (both lists of device tensors)."""
+    M = shards[0].shape[0] if M is None else M
+    GatherCall(h, shards, outs, M, stream)()
+
+
+def hg_gather_host(h: Handle, shards: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
+                   M: int | None = None, stream=None) -> None:
+    """One gather whose shards and outputs are page-locked host tensors
+    (``tensor.pin_memory()``) or device tensors: the kernel reads and writes
+    host memory directly."""
     M = shards[0].shape[0] if M is None else M
     GatherCall(h, shards, outs, M, stream)()
 
