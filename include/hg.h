@@ -69,7 +69,8 @@ typedef struct hg_options {
                                1, 2 or 4; default chosen per row count */
   int ctas;                 /* CTAs of the gather kernel (32 * tp threads each);
                                default chosen per row count; clamped to what is
-                               co-resident */
+                               co-resident. Also caps the grid of
+                               hg_gather_fused (default one CTA per SM) */
   int prefetch;             /* 0: chosen per row count (off unless tuned), 1: the
                                next push's shard loads are issued one iteration
                                ahead of its stores (overlapping a poll), 2: off */

@@ -64,15 +64,21 @@ def unfused_equal(outs, logits, M):
     assert torch.equal(outs[0].view(torch.int32), want)
 
 
-@pytest.mark.parametrize("tp,W,K,Ms", [
-    (2, 256, 128, [1, 3]),       # two tiles per rank, two K blocks
-    (2, 256, 1024, [8, 8]),      # 16 K blocks: every smem stage reused twice
-    (3, 384, 192, [16, 2]),      # odd TP, N fully used (M = 16)
-    (1, 128, 64, [5, 1]),        # degenerate TP=1, one tile, one K block
-    (4, 1280, 576, [4, 7, 1]),   # ten tiles per rank over the grid
+@pytest.mark.parametrize("tp,W,K,Ms,ctas", [
+    (2, 256, 128, [1, 3], 0),       # two tiles per rank, two K blocks
+    (2, 256, 1024, [8, 8], 0),      # 16 K blocks: every smem stage reused twice
+    (3, 384, 192, [16, 2], 0),      # odd TP, N fully used (M = 16)
+    (1, 128, 64, [5, 1], 0),        # degenerate TP=1, one tile, one K block
+    (4, 1280, 576, [4, 7, 1], 0),   # ten tiles per rank over the grid
+    # forced grids: 16 tiles over G CTAs, the tail split along K
+    (2, 1024, 576, [3, 1], 12),     # 1 full wave + 4 tail tiles in 3 parts each
+    (2, 1024, 576, [8], 7),         # 2 full waves + 2 tail tiles in 3 parts
+    (2, 1024, 576, [2, 5], 5),      # 3 full waves + 1 tail tile in 4 parts
+    (2, 1024, 128, [4], 5),         # 2 K blocks: the split stops at 2 parts
+    (2, 1024, 576, [6], 10),        # tail of 6 > half the grid: not split
 ])
-def test_fused_small_vs_oracle(tp, W, K, Ms):
-    h = hg.hg_create(tp, W, 16)
+def test_fused_small_vs_oracle(tp, W, K, Ms, ctas):
+    h = hg.hg_create(tp, W, 16, ctas=ctas)
     weight_cpu = [synth.weight(4, r, W, K) for r in range(tp)]
     weight = [w.cuda() for w in weight_cpu]
     for call, M in enumerate(Ms):

@@ -27,13 +27,25 @@
 // word into all TP mailboxes. The GEMM streams each weight byte from HBM once
 // (evict-first), so the kernel is bound by HBM bandwidth on the weights.
 //
-// Gather. Tiles are dealt round-robin to the CTAs (one CTA per SM, all
-// co-resident: cooperative launch). After its own tiles, CTA g polls the
-// tiles of CTA g+1 (mod G) in every rank's mailbox, copies them to the
-// outputs and re-arms, as the gather kernel does. Every wait in this kernel
-// (mbarriers and polls) is bounded by %globaltimer; on expiry the kernel
-// records the error in the status block, lets its in-flight copies and MMAs
-// drain, frees its tensor memory and returns.
+// Tail split. Tiles are dealt round-robin to the CTAs (one CTA per SM, all
+// co-resident: cooperative launch): every CTA takes full_waves whole tiles.
+// The tail tiles left over (fewer than the CTAs) would leave most SMs idle
+// while a few stream one more tile, so when there are at most half as many
+// tail tiles as CTAs each is split along K into `split` parts on `split`
+// CTAs. The part-0 CTA (the owner) keeps its fp32 partial in registers; every
+// other part writes its partial [128 x M] into a split cell, and the owner
+// polls the cell, adds it, re-arms the cell, rounds and pushes. A split cell
+// is a Lamport cell like a mailbox row: armed with 0xffffffff in every word
+// (a NaN that the accumulation never produces; a partial with that bit
+// pattern is written as the NaN 0x7fffffff instead), written with relaxed
+// stores, polled until no armed word is left, and re-armed by its reader.
+//
+// Gather. After its own tiles, CTA g polls the tiles that CTA g+1 (mod G)
+// pushed (its whole tiles and the tail tile it owns) in every rank's mailbox,
+// copies them to the outputs and re-arms, as the gather kernel does. Every
+// wait in this kernel (mbarriers and polls) is bounded by %globaltimer; on
+// expiry the kernel records the error in the status block, lets its
+// in-flight copies and MMAs drain, frees its tensor memory and returns.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -54,6 +66,7 @@ constexpr uint32_t kBBytes = kMmaN * kBlockK * 2;   // 2048
 constexpr int kAccCols = 16;     // fp32 columns of one accumulator
 constexpr uint32_t kTmemCols = 32;  // two accumulators (power of two >= 32)
 constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kPollBatch = 8;    // gather phase: mailbox vectors per thread in flight
 constexpr size_t kSmemBytes = (size_t)kStages * (kABytes + kBBytes) + 1024 /*align*/ + 256;
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
@@ -219,6 +232,8 @@ struct Shared {
   uint32_t tmem_base;
   uint32_t failed;
 };
+static_assert(sizeof(Shared) <= 256, "barriers must fit the 256 bytes kept after the stages");
+static_assert(kSmemBytes <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
 
 __device__ __forceinline__ void raise_error(const FusedArgs& a, int where) {
   if (atomicCAS(a.status, kDevOk, kDevTimeout) == kDevOk) {
@@ -240,6 +255,95 @@ __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FusedArgs& a, in
       return false;
     }
   }
+}
+
+// One work item of a CTA: a tile (rank r's vocab rows t * 128 ..) and the
+// K-block range [kb0, kb1) it covers; part -1 for a whole tile, else the
+// part of split tail tile j.
+struct Item {
+  int tile, kb0, kb1, part, j;
+};
+
+// Work items of CTA g: full_waves whole tiles, then at most one tail item.
+__device__ __forceinline__ int item_count(const FusedArgs& a, int g) {
+  const bool tail = a.split <= 1 ? g < a.tail : g < a.tail * a.split;
+  return a.full_waves + (tail ? 1 : 0);
+}
+
+__device__ __forceinline__ Item item_at(const FusedArgs& a, int g, int G, int i, int kblocks) {
+  if (i < a.full_waves) return Item{g + i * G, 0, kblocks, -1, -1};
+  if (a.split <= 1) return Item{a.full_waves * G + g, 0, kblocks, -1, -1};
+  const int j = g / a.split, p = g - j * a.split;
+  return Item{a.full_waves * G + j, p * kblocks / a.split, (p + 1) * kblocks / a.split, p, j};
+}
+
+// Words of split cell (tail tile j, part p >= 1) for vocab row `row`.
+__device__ __forceinline__ uint32_t* split_cell(const FusedArgs& a, int j, int p, int row) {
+  return a.split_cells + ((size_t)(j * (a.split - 1) + (p - 1)) * 128 + (size_t)row) * 16;
+}
+
+// Tiles CTA c pushed (its whole tiles, then the tail tile it owns, if any):
+// count, and the k-th of them.
+__device__ __forceinline__ int own_tail_of(const FusedArgs& a, int c, int G) {
+  if (a.split <= 1) return c < a.tail ? a.full_waves * G + c : -1;
+  return (c % a.split == 0 && c / a.split < a.tail) ? a.full_waves * G + c / a.split : -1;
+}
+
+// Poll tile `it` (pushed by another CTA) in every rank's mailbox until it has
+// arrived, copy it to the outputs and re-arm it: this thread's share is
+// vectors tid, tid + nthr, ..., kPollBatch of them in flight at once. False
+// when a poll gave up (recorded in the status block).
+__device__ bool consume_tile(const FusedArgs& a, int it, size_t parity_off, int tid, int nthr) {
+  const int V = a.tp * a.W;
+  const int per_row = kTileN / 8;                  // 16-byte vectors of a tile row
+  const int per_item = a.tp * a.M * per_row;       // 16-byte vectors of a tile, all ranks
+  const int r = it / a.tiles_per_rank;
+  const int t = it - r * a.tiles_per_rank;
+  const uint4 sent = make_uint4(kSentinel, kSentinel, kSentinel, kSentinel);
+  // Vector j: rank d's mailbox, row m, 16-byte vector vv of the tile.
+  auto word_off = [&](int j, int* d) {
+    *d = j / (a.M * per_row);
+    const int rem = j - *d * (a.M * per_row);
+    const int m = rem / per_row;
+    const int vv = rem - m * per_row;
+    return (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + (size_t)t * (kTileN / 2) +
+           (size_t)vv * 4;  // in words
+  };
+  for (int base = tid; base < per_item; base += nthr * kPollBatch) {
+    uint4 x[kPollBatch];
+#pragma unroll
+    for (int k = 0; k < kPollBatch; ++k) {
+      const int j = base + k * nthr;
+      if (j < per_item) {
+        int d;
+        const size_t off = word_off(j, &d);
+        x[k] = ld_poll_v4(reinterpret_cast<const uint4*>(
+            reinterpret_cast<const uint32_t*>(a.box[d]) + parity_off + off));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPollBatch; ++k) {
+      const int j = base + k * nthr;
+      if (j >= per_item) continue;
+      int d;
+      const size_t off = word_off(j, &d);
+      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off);
+      if (!arrived_v4(x[k])) {
+        const unsigned long long t0 = globaltimer_ns();
+        do {
+          x[k] = ld_poll_v4(p);
+          if (arrived_v4(x[k])) break;
+          if (globaltimer_ns() - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+            raise_error(a, 6);
+            return false;
+          }
+        } while (true);
+      }
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.out[d]) + off) = x[k];
+      st_relaxed_v4(p, sent);
+    }
+  }
+  return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ FusedArgs a) {
@@ -286,10 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
 
-  const int items = a.tp * a.tiles_per_rank;
   const int G = (int)gridDim.x;
   const int g = (int)blockIdx.x;
   const int kblocks = a.K / kBlockK;
+  const int n_items = item_count(a, g);
+  // The CTA whose pushes this one consumes, and its tiles.
+  const int cons = (g + 1 == G) ? 0 : g + 1;
+  const int cons_tail = own_tail_of(a, cons, G);
+  const int n_cons = a.full_waves + (cons_tail >= 0 ? 1 : 0);
+  auto cons_tile = [&](int k) { return k < a.full_waves ? cons + k * G : cons_tail; };
 
   if (warp == 0) {
     // TMA producer.
@@ -299,10 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int it = g; it < items && ok; it += G) {
-        const int r = it / a.tiles_per_rank;
-        const int t = it - r * a.tiles_per_rank;
-        for (int kb = 0; kb < kblocks; ++kb) {
+      for (int i = 0; i < n_items && ok; ++i) {
+        const Item w = item_at(a, g, G, i, kblocks);
+        const int r = w.tile / a.tiles_per_rank;
+        const int t = w.tile - r * a.tiles_per_rank;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(&sh->empty[stage], phase ^ 1u, a, 1)) { ok = false; break; }
           mbar_expect_tx(&sh->full[stage], kABytes + kBBytes);
           tma_load_2d(sA + (size_t)stage * kABytes, &a.tm_w[r], kb * kBlockK, t * kTileN,
@@ -321,11 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int it = g; it < items && ok; it += G) {
+      for (int i = 0; i < n_items && ok; ++i) {
+        const Item w = item_at(a, g, G, i, kblocks);
         if (!mbar_wait(&sh->acc_empty[acc], acc_phase ^ 1u, a, 2)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(&sh->full[stage], phase, a, 3)) { ok = false; break; }
           tc_fence_after();
           const uint64_t adesc = smem_desc_sw128(smem_u32(sA + (size_t)stage * kABytes));
@@ -334,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
           for (int k = 0; k < kBlockK / kMmaK; ++k) {
             // K step of 16 bf16 = 32 bytes = 2 in the start-address field.
             mma_bf16_f32(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
-                         (kb | k) != 0 ? 1u : 0u);
+                         (kb != w.kb0 || k != 0) ? 1u : 0u);
           }
           mma_commit(&sh->empty[stage]);  // stage free once these MMAs have read it
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -354,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     const int V = a.tp * a.W;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int it = g; it < items; it += G) {
+    for (int i = 0; i < n_items; ++i) {
+      const Item w = item_at(a, g, G, i, kblocks);
       // Every lane waits; the vote reconverges the warp before the warp-wide
       // tcgen05.ld and makes the give-up decision the same for all lanes.
       const bool ready = mbar_wait(&sh->acc_full[acc], acc_phase, a, 5);
@@ -367,25 +479,82 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
 
-      const int r = it / a.tiles_per_rank;
-      const int t = it - r * a.tiles_per_rank;
-      // Word of vocab columns (row, row + 1) of rank r, for even rows.
-      const size_t wcol = (size_t)t * (kTileN / 2) + (size_t)(row >> 1);
-      uint32_t* lg = reinterpret_cast<uint32_t*>(a.logits[r]);
+      const int nvec = (a.M + 3) / 4;  // 16-byte vectors of a cell row that hold rows m < M
+      if (w.part > 0) {
+        // A later part of a split tail tile: hand the fp32 partial to part 0.
+        uint32_t* c = split_cell(a, w.j, w.part, row);
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        if (m < a.M) {
-          const float mine = __uint_as_float(v[m]);
-          const float next = __shfl_down_sync(0xffffffffu, mine, 1);
-          if ((lane & 1) == 0) {
-            const uint32_t word = pack_bf16x2(mine, next);  // low half = even column
-            if (lg) lg[(size_t)m * (a.W / 2) + wcol] = word;
-            const uint32_t y = word == kSentinel ? kSentAs : word;
-            const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + wcol;
-            for (int d = 0; d < a.tp; ++d)
-              st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off, y);
+        for (int q = 0; q < 4; ++q) {
+          if (q < nvec) {
+            uint4 x;
+            x.x = v[4 * q] == kSplitArmed ? kSplitArmedAs : v[4 * q];
+            x.y = v[4 * q + 1] == kSplitArmed ? kSplitArmedAs : v[4 * q + 1];
+            x.z = v[4 * q + 2] == kSplitArmed ? kSplitArmedAs : v[4 * q + 2];
+            x.w = v[4 * q + 3] == kSplitArmed ? kSplitArmedAs : v[4 * q + 3];
+            st_relaxed_v4(reinterpret_cast<uint4*>(c) + q, x);
           }
         }
+      } else {
+        if (w.part == 0) {
+          // Part 0 of a split tail tile: add the other parts' partials (in part
+          // order), polling their cells, and re-arm the cells.
+          bool got = true;
+          for (int p = 1; p < a.split && got; ++p) {
+            uint4* c = reinterpret_cast<uint4*>(split_cell(a, w.j, p, row));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (q < nvec && got) {
+                uint4 x = ld_poll_v4(c + q);
+                const unsigned long long t0 = globaltimer_ns();
+                while (x.x == kSplitArmed || x.y == kSplitArmed || x.z == kSplitArmed ||
+                       x.w == kSplitArmed) {
+                  if (globaltimer_ns() - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+                    raise_error(a, 7);
+                    got = false;
+                    break;
+                  }
+                  x = ld_poll_v4(c + q);
+                }
+                if (got) {
+                  v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + __uint_as_float(x.x));
+                  v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + __uint_as_float(x.y));
+                  v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + __uint_as_float(x.z));
+                  v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + __uint_as_float(x.w));
+                  st_relaxed_v4(c + q, make_uint4(kSplitArmed, kSplitArmed, kSplitArmed, kSplitArmed));
+                }
+              }
+            }
+          }
+          if (!__all_sync(0xffffffffu, got)) break;
+        }
+
+        const int r = w.tile / a.tiles_per_rank;
+        const int t = w.tile - r * a.tiles_per_rank;
+        // Word of vocab columns (row, row + 1) of rank r, for even rows.
+        const size_t wcol = (size_t)t * (kTileN / 2) + (size_t)(row >> 1);
+        uint32_t* lg = reinterpret_cast<uint32_t*>(a.logits[r]);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          if (m < a.M) {
+            const float mine = __uint_as_float(v[m]);
+            const float next = __shfl_down_sync(0xffffffffu, mine, 1);
+            if ((lane & 1) == 0) {
+              const uint32_t word = pack_bf16x2(mine, next);  // low half = even column
+              if (lg) lg[(size_t)m * (a.W / 2) + wcol] = word;
+              const uint32_t y = word == kSentinel ? kSentAs : word;
+              const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + wcol;
+              for (int d = 0; d < a.tp; ++d)
+                st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off, y);
+            }
+          }
+        }
+      }  // whole tile or part 0
+      // One item behind, the gather of the neighbour's tiles: its item i - 1
+      // was pushed about one tile of weight streaming ago, so these polls
+      // rarely wait, and the copy overlaps this CTA's next tile.
+      if (i >= 1 && i - 1 < n_cons) {
+        const bool ok = consume_tile(a, cons_tile(i - 1), parity_off, (int)threadIdx.x - 64, 128);
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
     }
   }
@@ -421,38 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   }
   if (failed) return;
 
-  // Gather: poll the tiles of CTA g+1 in every rank's mailbox, copy, re-arm.
-  const int cons = (g + 1 == G) ? 0 : g + 1;
-  const int V = a.tp * a.W;
-  const int per_item = a.tp * a.M * (kTileN / 8);  // 16-byte vectors per tile
-  const uint4 sent = make_uint4(kSentinel, kSentinel, kSentinel, kSentinel);
-  for (int it = cons; it < items; it += G) {
-    const int r = it / a.tiles_per_rank;
-    const int t = it - r * a.tiles_per_rank;
-    for (int j = (int)threadIdx.x; j < per_item; j += kThreads) {
-      const int d = j / (a.M * (kTileN / 8));
-      const int rem = j - d * (a.M * (kTileN / 8));
-      const int m = rem / (kTileN / 8);
-      const int vv = rem - m * (kTileN / 8);
-      const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + (size_t)t * (kTileN / 2) +
-                         (size_t)vv * 4;  // in words
-      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off);
-      uint4 x = ld_poll_v4(p);
-      if (!arrived_v4(x)) {
-        const unsigned long long t0 = globaltimer_ns();
-        do {
-          x = ld_poll_v4(p);
-          if (arrived_v4(x)) break;
-          if (globaltimer_ns() - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
-            raise_error(a, 6);
-            return;
-          }
-        } while (true);
-      }
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.out[d]) + off) = x;
-      st_relaxed_v4(p, sent);
-    }
-  }
+  // The rest of the gather: the neighbour's tiles the epilogue loop has not
+  // consumed (its last one or two), by every thread.
+  for (int k = n_items >= 1 ? n_items - 1 : 0; k < n_cons; ++k)
+    if (!consume_tile(a, cons_tile(k), parity_off, (int)threadIdx.x, kThreads)) return;
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -497,6 +638,11 @@ int fused_limits(int* max_tp, int* max_m, int* k_multiple, int* w_multiple) {
   return 0;
 }
 
+size_t split_cells_needed(int sms) {
+  // tail * (split - 1) < tail * split <= grid <= one CTA per SM
+  return (size_t)(sms > 0 ? sms : 1);
+}
+
 cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   FusedArgs a;  // copied into the launch by cudaLaunchKernelExC
   static bool attr_set = false;
@@ -536,7 +682,24 @@ cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int grid = sms * per_sm;
+  if (l.max_ctas > 0 && grid > l.max_ctas) grid = l.max_ctas;
   if (grid > items) grid = items;
+  // Work split: whole tiles in full waves; a tail of at most half the grid is
+  // split along K (at most kMaxSplit parts, each of at least one K block) if
+  // the handle has split cells for it.
+  a.full_waves = items / grid;
+  a.tail = items - a.full_waves * grid;
+  a.split = 1;
+  a.split_cells = nullptr;
+  if (a.tail > 0 && 2 * a.tail <= grid && l.split_cells) {
+    int split = grid / a.tail;
+    if (split > kMaxSplit) split = kMaxSplit;
+    if (split > l.K / kBlockK) split = l.K / kBlockK;
+    if (split >= 2 && (size_t)a.tail * (split - 1) <= l.split_cell_count) {
+      a.split = split;
+      a.split_cells = l.split_cells;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);

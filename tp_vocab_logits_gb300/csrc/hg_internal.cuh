@@ -107,7 +107,26 @@ struct FusedArgs {
   int* parity_words;
   int parity_entries;
   size_t parity_stride_words;
+  // Work split: every CTA takes full_waves whole tiles (tiles g + k * G);
+  // the `tail` remaining tiles are split along K into `split` parts (split
+  // 1: tail tile j is taken whole by CTA j). Part p of tail tile j runs on
+  // CTA j * split + p; parts 1.. hand their fp32 partials to part 0 through
+  // split_cells ([tail][split - 1][128 rows][16] words, armed with
+  // kSplitArmed).
+  int full_waves;
+  int tail;
+  int split;
+  uint32_t* split_cells;
 };
+
+// Armed word of a split cell, and the word a partial with that bit pattern
+// is written as (both NaNs).
+constexpr uint32_t kSplitArmed = 0xffffffffu;
+constexpr uint32_t kSplitArmedAs = 0x7fffffffu;
+// Words of one split cell (128 rows x 16 fp32 columns) and the most parts a
+// tail tile is split into.
+constexpr size_t kSplitCellWords = 128 * 16;
+constexpr int kMaxSplit = 4;
 
 // Host-side description of one fused call.
 struct FusedLaunch {
@@ -122,6 +141,9 @@ struct FusedLaunch {
   int* parity_words = nullptr;  // device-resident parity copies (nullptr: box[] resolved)
   int parity_entries = 0;
   size_t parity_stride_words = 0;
+  uint32_t* split_cells = nullptr;  // armed split cells (nullptr: tail tiles are not split)
+  size_t split_cell_count = 0;      // cells available (each kSplitCellWords words)
+  int max_ctas = 0;                 // cap on the grid (0: one CTA per SM)
 };
 
 // Limits of the fused path: TP, rows, K granularity, W granularity.
@@ -129,6 +151,9 @@ int fused_limits(int* max_tp, int* max_m, int* k_multiple, int* w_multiple);
 
 // Cooperative launch of the fused kernel (one CTA per SM at most).
 cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms);
+
+// Split cells a handle needs for any fused call on a device with `sms` SMs.
+size_t split_cells_needed(int sms);
 
 }  // namespace fused
 

@@ -41,6 +41,9 @@ struct hg_handle {
   std::vector<int> chunks_stats;
   hg::RowPartial* partials = nullptr;  // statistics cells: one per unit of the largest call
   size_t partial_count = 0;
+  uint32_t* split_cells = nullptr;  // fused calls: split cells of the tail tiles (armed)
+  size_t split_cell_count = 0;
+  int max_ctas = 0;                 // hg_options.ctas: also caps the fused grid
 };
 
 namespace {
@@ -58,6 +61,7 @@ void free_handle(hg_handle* h) {
   if (h->status) cudaFree(h->status);
   if (h->parity_words) cudaFree(h->parity_words);
   if (h->partials) cudaFree(h->partials);
+  if (h->split_cells) cudaFree(h->split_cells);
   delete h;
 }
 
@@ -192,6 +196,7 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
   h->timeout_ns = opt && opt->poll_timeout_ns ? opt->poll_timeout_ns : kDefaultTimeoutNs;
   h->cooperative = opt && opt->cooperative;
   h->device_parity = opt && opt->device_parity;
+  h->max_ctas = opt ? opt->ctas : 0;
 
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -224,6 +229,22 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
                             hg::kSentinel, nullptr) != cudaSuccess) {
       free_handle(h);
       return HG_ERR_CUDA;
+    }
+  }
+  {
+    // Split cells of the fused producer's tail tiles, armed (handles whose
+    // shape the fused call accepts).
+    int max_tp = 0, max_m = 0, k_mult = 0, w_mult = 0;
+    hg::fused::fused_limits(&max_tp, &max_m, &k_mult, &w_mult);
+    if (tp <= max_tp && h->vec16 && shard_cols % w_mult == 0) {
+      h->split_cell_count = hg::fused::split_cells_needed(h->sms);
+      const size_t words = h->split_cell_count * hg::fused::kSplitCellWords;
+      if (cudaMalloc(&h->split_cells, words * sizeof(uint32_t)) != cudaSuccess ||
+          hg::launch_fill_u32(h->split_cells, words, hg::fused::kSplitArmed, nullptr) !=
+              cudaSuccess) {
+        free_handle(h);
+        return HG_ERR_CUDA;
+      }
     }
   }
   if (cudaMalloc(&h->status, hg::kStatusWords * sizeof(int)) != cudaSuccess ||
@@ -567,6 +588,10 @@ int hg_rearm(hg_handle* h, hg_stream_t stream) {
       hg::launch_fill_u32(reinterpret_cast<uint32_t*>(h->partials), h->partial_count * 4,
                           hg::kSentinel, stream) != cudaSuccess)
     return HG_ERR_CUDA;
+  if (h->split_cells &&
+      hg::launch_fill_u32(h->split_cells, h->split_cell_count * hg::fused::kSplitCellWords,
+                          hg::fused::kSplitArmed, stream) != cudaSuccess)
+    return HG_ERR_CUDA;
   h->parity = 0;
   h->failed = false;
   return HG_OK;
@@ -641,6 +666,9 @@ int hg_gather_fused(hg_handle* h, const void* const* hidden_ptrs, const void* co
   l.W = h->W;
   l.K = K;
   l.M = M;
+  l.split_cells = h->split_cells;
+  l.split_cell_count = h->split_cell_count;
+  l.max_ctas = h->max_ctas;
   if (hg::fused::fused_launch(l, stream, h->sms) != cudaSuccess) return HG_ERR_CUDA;
   if (!h->device_parity) h->parity ^= 1;
   return HG_OK;
