@@ -299,32 +299,43 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a) {
     float mx = kNegInf, s = 0.f;
     int arg = 0x7fffffff;
     bool gave_up = false;
-    for (int base = lane; base < per_row; base += kCellBatch * 32) {
-      // Issue a batch of cell loads first, so that their latencies overlap.
+    for (int base = lane; base < per_row && !gave_up; base += kCellBatch * 32) {
+      // A batch of cells in flight; the ones still armed are re-loaded
+      // together (never one at a time), until all have arrived (bounded).
       uint4 v[kCellBatch];
-#pragma unroll
-      for (int k = 0; k < kCellBatch; ++k)
-        if (base + 32 * k < per_row) v[k] = Elem<uint4>::ld_poll(q + base + 32 * k);
+      unsigned todo = 0;
 #pragma unroll
       for (int k = 0; k < kCellBatch; ++k) {
-        const int j = base + 32 * k;
-        if (j >= per_row || gave_up) continue;
-        if (!Elem<uint4>::arrived(v[k])) {
-          const unsigned long long t0 = globaltimer_ns();
-          do {
-            v[k] = Elem<uint4>::ld_poll(q + j);
-            if (Elem<uint4>::arrived(v[k])) break;
-            if (globaltimer_ns() - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
-              record_timeout(a, -1, -1, (size_t)j);
-              gave_up = true;
-              break;
-            }
-          } while (true);
-          if (gave_up) continue;
+        if (base + 32 * k < per_row) {
+          v[k] = Elem<uint4>::ld_poll(q + base + 32 * k);
+          todo |= 1u << k;
         }
+      }
+      const unsigned valid = todo;
+      unsigned long long t0 = 0;
+      for (;;) {
+#pragma unroll
+        for (int k = 0; k < kCellBatch; ++k)
+          if ((todo >> k & 1) && Elem<uint4>::arrived(v[k])) todo &= ~(1u << k);
+        if (!todo) break;
+        const unsigned long long now = globaltimer_ns();
+        if (t0 == 0) t0 = now;
+        if (now - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+          record_timeout(a, -1, -1, (size_t)base);
+          gave_up = true;
+          break;
+        }
+#pragma unroll
+        for (int k = 0; k < kCellBatch; ++k)
+          if (todo >> k & 1) v[k] = Elem<uint4>::ld_poll(q + base + 32 * k);
+      }
+      if (gave_up) break;
+#pragma unroll
+      for (int k = 0; k < kCellBatch; ++k) {
+        if (!(valid >> k & 1)) continue;
         combine_partial(mx, arg, s, __uint_as_float(v[k].x), (int)v[k].y,
                         __uint_as_float(v[k].z));
-        Elem<uint4>::st_relaxed(q + j, armed);
+        Elem<uint4>::st_relaxed(q + base + 32 * k, armed);
       }
     }
 #pragma unroll
