@@ -471,25 +471,30 @@ def run_ours(args):
     del shards, outs, calls
 
     # ---- per-M (config 3 row counts) and large M ----
-    per_m, per_m_shape, per_m_graph, per_m_graph_tuned, per_m_tuned_shape = {}, {}, {}, {}, {}
+    per_m, per_m_tuned, per_m_shape, per_m_tuned_shape = {}, {}, {}, {}
+    per_m_graph, per_m_graph_tuned = {}, {}
     if not args.quick:
         for M in range(1, 9):
             n = sets_for(TP, W, M)
-            hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, CAP, M, n, device,
-                                              rows=[M], seed=2, autotune=tune)
-            t = time_calls(torch, cm_, 200, 20, stream)
-            hg.hg_sync(hm)
-            per_m[str(M)] = round(t * 1000.0 / 200, 3)
-            per_m_shape[str(M)] = hg.hg_launch_shape(hm, M)
-            hm.close()
-            del sm_, om_, cm_
+            # calls issued one by one from Python: fixed rule, then shapes timed
+            # at hg_create
+            for tuned, res, shp in ((False, per_m, per_m_shape),
+                                    (True, per_m_tuned, per_m_tuned_shape)):
+                hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, CAP, M, n, device,
+                                                  rows=[M], seed=2, autotune=tuned)
+                t = time_calls(torch, cm_, 200, 20, stream)
+                hg.hg_sync(hm)
+                res[str(M)] = round(t * 1000.0 / 200, 3)
+                shp[str(M)] = hg.hg_launch_shape(hm, M)
+                hm.close()
+                del sm_, om_, cm_
             # host-free issue: 200 calls captured once, replayed (fixed rule, then
             # shapes timed at hg_create)
             per_m_graph[str(M)] = graph_replay_us(torch, hg, synth, TP, W, CAP, M, device,
                                                   stream, 1000, rows=[M], seed=2)
-            per_m_graph_tuned[str(M)], per_m_tuned_shape[str(M)] = graph_replay_us(
+            per_m_graph_tuned[str(M)] = graph_replay_us(
                 torch, hg, synth, TP, W, CAP, M, device, stream, 1000, rows=[M], seed=2,
-                autotune=True, with_shape=True)
+                autotune=True)
     large = {}
     for M in ([] if args.quick else [64, 128, 256]):
         hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, M, M, 3, device, rows=[M],
@@ -566,9 +571,10 @@ def run_ours(args):
                              "L2-resident and the launch is latency-bound"},
         "per_m": per_m,
         "per_m_launch": per_m_shape,
+        "per_m_autotuned": per_m_tuned,
+        "per_m_autotuned_launch": per_m_tuned_shape,
         "per_m_graph_replay": per_m_graph,
         "per_m_graph_replay_autotuned": per_m_graph_tuned,
-        "per_m_autotuned_launch": per_m_tuned_shape,
         "large_m": large,
         "with_row_stats_us_per_call": stats_us,
         "gather_then_torch_row_stats_us_per_call": torch_stats_us,
