@@ -213,6 +213,16 @@ def make_workload(torch, hg, synth, tp, W, cap, M, sets, device, rows=None, seed
     return h, shards, outs, calls
 
 
+def check_concat(torch, shards, outs, tp, what):
+    """outs[d] equals the rank-order concat of the shards with the sentinel
+    word rewritten to (+0, +0), for every rank d (checked on the device)."""
+    want = torch.cat([shards[r].view(torch.int32) for r in range(tp)], dim=1)
+    want = torch.where(want == -(1 << 31), torch.zeros_like(want), want)
+    for d in range(tp):
+        if not torch.equal(outs[d].view(torch.int32), want):
+            raise SystemExit(f"bench: {what}: output of rank {d} wrong")
+
+
 def sets_for(tp, W, M, minimum=3) -> int:
     per = M * tp * W * 2 * (1 + tp)  # shard + output bytes of one set
     return max(minimum, -(-2 * L2_BYTES // per))
@@ -677,8 +687,14 @@ def run_sweep(args):
                                               prefetch=args.prefetch,
                                               cooperative=args.cooperative,
                                               autotune=args.autotune)
+                c_[0]()  # first call of the point, checked before timing
+                hg.hg_sync(h)
+                check_concat(torch, s_[0], o_[0], tp, f"sweep tp={tp} W={Wd} M={M} first call")
                 t = time_calls(torch, c_, args.calls, 10, stream)
                 hg.hg_sync(h)
+                last = (args.calls - 1) % n  # set of the last timed call
+                check_concat(torch, s_[last], o_[last], tp,
+                             f"sweep tp={tp} W={Wd} M={M} last call")
                 us = t * 1000.0 / args.calls
                 gbs = algorithmic_bytes(tp, Wd, M) / (us * 1e-6) / 1e9
                 print(json.dumps({"sweep": "bandwidth", "tp": tp, "shard_cols": Wd, "M": M,
