@@ -1,6 +1,7 @@
 """Graph-capturable gather: handles created with device_parity keep the parity
-in device memory (each call's kernel reads it, the last CTA flips it), so calls
-may be captured into a CUDA graph and replayed. Parity with the CPU oracle as
+in device memory (each reader of a call's kernel reads its own copy of it, and
+every copy is flipped once per call after it was read), so calls may be
+captured into a CUDA graph and replayed. Parity with the CPU oracle as
 everywhere: outputs word for word, mailboxes re-armed, parity sequence."""
 
 import numpy as np
@@ -78,11 +79,14 @@ def _eager(h, shards, outs, M):
     return from_dev(outs)
 
 
-def test_fused_graph_capture_replay():
+@pytest.mark.parametrize("ctas", [0, 5])
+def test_fused_graph_capture_replay(ctas):
     """The fused LM-head producer on a device-parity handle, captured and
-    replayed: outputs equal the unfused gather of its own logits each replay."""
+    replayed: outputs equal the unfused gather of its own logits each replay.
+    With 5 CTAs the 16 tiles leave one tail tile split into 4 parts, whose
+    split cells must be re-armed by every replay."""
     tp, W, K, M = 4, 512, 256, 3
-    h = hg.hg_create(tp, W, 4, device_parity=True)
+    h = hg.hg_create(tp, W, 4, device_parity=True, ctas=ctas)
     weight = [synth.weight(8, r, W, K, device="cuda") for r in range(tp)]
     hid = synth.hidden(8, tp, M, K, device="cuda")
     hidden = [hid[r] for r in range(tp)]
@@ -111,3 +115,35 @@ def test_fused_graph_capture_replay():
         assert_mailboxes_armed(h, hg)
     h.close()
     h2.close()
+
+
+def test_host_buffers_graph_replay_vs_oracle():
+    """hg_gather_host on a device-parity handle, captured once (two calls) and
+    replayed twice: page-locked host outputs against the oracle run through
+    the same four calls."""
+    tp, W, cap, M = 4, 1024, 2, 2
+    h = hg.hg_create(tp, W, cap, device_parity=True)
+    og = oracle.Gather(tp, W, cap)
+    sets = [synth.shards(31, tp, M, W, scale=3.0, sent_frac=0.02, set_index=i)
+            .numpy().view(np.uint16) for i in range(2)]
+    shards = [[torch.from_numpy(b[r].view(np.int16).copy()).pin_memory() for r in range(tp)]
+              for b in sets]
+    outs = [[torch.zeros((M, tp * W), dtype=torch.int16).pin_memory() for _ in range(tp)]
+            for _ in range(2)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(2):
+            hg.hg_gather_host(h, shards[i], outs[i], M, stream=s)
+    for replay in range(2):
+        wants = [og.call(sets[i]) for i in range(2)]
+        g.replay()
+        torch.cuda.synchronize()
+        hg.hg_sync(h)
+        for i in range(2):
+            got = np.stack([o.numpy().view(np.uint16) for o in outs[i]])
+            np.testing.assert_array_equal(got, wants[i], err_msg=f"replay {replay} call {i}")
+        assert hg.hg_parity(h) == og.parity
+    assert_mailboxes_armed(h, hg)
+    h.close()
