@@ -66,7 +66,8 @@ enum {
 typedef struct hg_options {
   uint64_t poll_timeout_ns; /* bound of every poll; default 1e9 (1 s) */
   int elems_per_lane;       /* 16-byte vectors (or words) per lane per unit:
-                               1, 2 or 4; default chosen per row count */
+                               1 to 6 for tp <= 16, 1 or 2 above; default
+                               chosen per row count */
   int ctas;                 /* CTAs of the gather kernel (32 * tp threads each);
                                default chosen per row count; clamped to what is
                                co-resident. Also caps the grid of
@@ -88,7 +89,9 @@ typedef struct hg_options {
   int autotune;             /* 0 (default): launch shapes from a fixed rule; 1:
                                hg_create_ex times candidate shapes (elements
                                per lane, CTAs, prefetch) of every served row
-                               count on the device and keeps the fastest. The
+                               count on the device and keeps the fastest
+                               (the fixed rule's shape unless another is
+                               faster by at least 3 %). The
                                candidates honour the fields above that are
                                set. The timed calls rotate over inputs and
                                outputs in a zero-filled pool of max(256 MB,

@@ -98,7 +98,9 @@ def test_parity_vs_oracle(tp, W, cap, Ms):
 
 @pytest.mark.parametrize("vpt,ctas,pref,coop", [
     (1, 1, 0, False), (1, 3, 1, False), (2, 7, 1, False), (4, 2, 2, False), (2, 0, 1, False),
-    (4, 0, 0, False), (1, 1, 1, False), (1, 0, 0, True), (4, 5, 1, True), (0, 0, 0, True)])
+    (4, 0, 0, False), (1, 1, 1, False), (3, 0, 0, False), (3, 5, 1, False), (5, 4, 1, False),
+    (6, 0, 0, False), (6, 2, 1, False), (1, 0, 0, True), (4, 5, 1, True), (3, 0, 0, True),
+    (0, 0, 0, True)])
 def test_launch_shapes_vs_oracle(vpt, ctas, pref, coop):
     """Forced launch shapes: small grids make every CTA loop over many units (a
     single CTA consumes its own pushes one iteration later); with and without
@@ -167,7 +169,7 @@ def test_autotuned_shapes_vs_oracle():
         assert hg.hg_parity(h) == 0
         for M in rows:
             s = hg.hg_launch_shape(h, M)
-            assert s["elems_per_lane"] in (1, 2, 4) and s["ctas"] >= 1
+            assert 1 <= s["elems_per_lane"] <= 6 and s["ctas"] >= 1
             assert s["threads"] == 32 * tp
         og = oracle.Gather(tp, W, cap, rows)
         _back_to_back(h, og, tp, W, synth.row_sequence(5, 14, rows), seed=12 + dp)
@@ -382,6 +384,18 @@ def test_create_rejects_bad_sizes():
         assert e.value.status == hg.HG_ERR_ARG
     with pytest.raises(hg.HGError):
         hg.hg_create(2, 64, 4, rows=[5])
+    for kw in ({"elems_per_lane": 7}, {"elems_per_lane": -1}, {"prefetch": 3}, {"ctas": -2}):
+        with pytest.raises(hg.HGError) as e:
+            hg.hg_create(2, 64, 4, **kw)
+        assert e.value.status == hg.HG_ERR_ARG
+    with pytest.raises(hg.HGError):
+        hg.hg_create(24, 64, 4, elems_per_lane=3)  # 1024-thread CTAs: 1 or 2 per lane
+    h = hg.hg_create(8, 20480, 8)
+    assert [hg.hg_launch_shape(h, M)["elems_per_lane"] for M in (1, 2, 3, 8)] == [3, 3, 4, 4]
+    h.close()
+    h = hg.hg_create(16, 4096, 2)
+    assert hg.hg_launch_shape(h, 1)["elems_per_lane"] == 4
+    h.close()
 
 
 def test_timeout_recovery():

@@ -478,16 +478,19 @@ __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
     p[i] = v;
 }
 
-// Kernels for tp <= 16 (CTAs of up to 512 threads) take 1, 2 or 4 elements
-// per lane; larger tp (up to 1024 threads, 64 registers) 1 or 2. Row
-// statistics exist for tp <= 16.
+// Kernels for tp <= 16 (CTAs of up to 512 threads) take 1 to 6 elements per
+// lane; larger tp (up to 1024 threads, 64 registers) 1 or 2. Row statistics
+// exist for tp <= 16.
 template <typename V, bool PREF, bool STATS>
 const void* pick_vpt(int vpt, int tp) {
   if (tp <= 16) {
     switch (vpt) {
       case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PREF, 512, STATS>);
       case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PREF, 512, STATS>);
+      case 3: return reinterpret_cast<const void*>(&gather_kernel<V, 3, PREF, 512, STATS>);
       case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4, PREF, 512, STATS>);
+      case 5: return reinterpret_cast<const void*>(&gather_kernel<V, 5, PREF, 512, STATS>);
+      case 6: return reinterpret_cast<const void*>(&gather_kernel<V, 6, PREF, 512, STATS>);
       default: return nullptr;
     }
   }

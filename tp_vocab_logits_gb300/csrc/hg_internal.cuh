@@ -72,6 +72,17 @@ struct LaunchShape {
   bool stats = false;  // the kernel also folds row statistics
 };
 
+// Elements per lane a gather kernel exists for: 1..6 for tp <= 16, 1..2 above.
+inline int max_vpt(int tp) { return tp <= 16 ? 6 : 2; }
+
+// Elements per lane of the fixed launch rule for M rows: 3 for one or two rows
+// at tp <= 8, where the call is latency-bound and smaller units put more
+// CTAs in flight; 4 otherwise (2 for tp > 16, whose CTAs have 1024 threads).
+inline int default_vpt(int tp, int M) {
+  if (tp > 16) return 2;
+  return (tp <= 8 && M <= 2) ? 3 : 4;
+}
+
 // Largest co-resident CTAs per SM of the gather kernel for this shape.
 cudaError_t gather_occupancy(const LaunchShape& s, bool vec16, int tp, int* ctas_per_sm);
 

@@ -66,21 +66,20 @@ void free_handle(hg_handle* h) {
 }
 
 // Launch shape for M rows by a fixed rule. One CTA = one warp per virtual
-// rank, each lane carrying the widest unit (4 elements per lane; 2 for CTAs of
-// 1024 threads); one CTA per unit up to the co-resident maximum, beyond which
-// the CTAs loop over the units; no prefetch. Measured at TP8, V=163840 (us/
-// call, M = 1, 2, 3, 4, 8, 64): 3.6, 5.7, 6.0, 7.4, 11.4, 90.8. Other shapes
-// win at some row counts (M = 2: 2 elements per lane on 456 CTAs, 4.7 us), and
-// no simple rule finds them, so hg_options.autotune times the candidates. The
-// grid never exceeds the co-resident CTA count, which the kernel's cross-CTA
-// polls need.
-int max_vpt_of(const hg_handle* h) { return h->tp <= 16 ? 4 : 2; }  // 1024-thread CTAs stop at 2
-
+// rank; each lane carries default_vpt(tp, M) elements (3 for one or two rows
+// at tp <= 8, 4 otherwise, 2 for CTAs of 1024 threads); one CTA per unit up to
+// the co-resident maximum, beyond which the CTAs loop over the units; no
+// prefetch. Measured at TP8, V=163840 (us/call, C loop): M=1 3.3 with 3
+// elements per lane against 3.6 with 4; M = 4, 8, 64: 7.5, 11.3, 90.3 with 4.
+// The best shape depends on tp, W and M in ways no simple rule captures (M=2:
+// 5 elements per lane, 4.5 us; M=64: 5, 87.4 us), so hg_options.autotune times
+// the candidates. The grid never exceeds the co-resident CTA count, which the
+// kernel's cross-CTA polls need.
 int check_shape_options(const hg_handle* h, const hg_options* opt) {
   if (!opt) return HG_OK;
   const int v = opt->elems_per_lane;
-  if (v != 0 && v != 1 && v != 2 && v != 4) return HG_ERR_ARG;
-  if (v > max_vpt_of(h) || opt->ctas < 0 || opt->prefetch < 0 || opt->prefetch > 2)
+  if (v < 0 || v > hg::max_vpt(h->tp) || opt->ctas < 0 || opt->prefetch < 0 ||
+      opt->prefetch > 2)
     return HG_ERR_ARG;
   if (opt->autotune < 0 || opt->autotune > 1) return HG_ERR_ARG;
   return HG_OK;
@@ -101,7 +100,10 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchS
   const int forced_ctas = opt ? opt->ctas : 0;
   hg::LaunchShape s;
   s.stats = stats;
-  s.vpt = forced_vpt ? forced_vpt : max_vpt_of(h);
+  // The statistics kernel keeps 4 elements per lane: its final reduction
+  // folds one cell per unit, and fewer, larger units measured faster (TP8,
+  // V=163840, M=1: 6.5 us with 4 per lane, 8.4 us with 3).
+  s.vpt = forced_vpt ? forced_vpt : (stats ? 4 : hg::default_vpt(h->tp, M));
   s.pref = opt && opt->prefetch == 1;
   const int chunks = (h->wv + 32 * s.vpt - 1) / (32 * s.vpt);
   const long long units = (long long)M * h->tp * chunks;
@@ -359,7 +361,7 @@ struct Candidate {
 int tune_candidates(hg_handle* h, int M, const hg_options* opt, std::vector<Candidate>* out) {
   std::vector<int> vpts;
   if (opt->elems_per_lane) vpts.push_back(opt->elems_per_lane);
-  else for (int v = 1; v <= max_vpt_of(h); v *= 2) vpts.push_back(v);
+  else for (int v = 1; v <= hg::max_vpt(h->tp); ++v) vpts.push_back(v);
   std::vector<bool> prefs;
   if (opt->prefetch == 0 || opt->prefetch == 2) prefs.push_back(false);
   if (opt->prefetch == 0 || opt->prefetch == 1) prefs.push_back(true);
@@ -410,6 +412,7 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
   constexpr size_t kPoolBytes = 256ull << 20;
   constexpr float kBlockUs = 300.f;
   constexpr int kRounds = 3;
+  constexpr float kMargin = 0.03f;
   const size_t V = (size_t)h->tp * h->W;
   // One set: tp shards [M][W], then tp outputs [M][V], each 16-byte aligned.
   auto set_bytes = [&](int M) { return (size_t)h->tp * M * (h->W + V) * 2; };
@@ -453,6 +456,9 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
     std::vector<Candidate> cand;
     rc = tune_candidates(h, M, opt, &cand);
     if (rc != HG_OK || cand.empty()) break;
+    Candidate fixed;  // the fixed rule's shape, as planned before tuning
+    fixed.s = h->shape[M];
+    fixed.chunks = h->chunks[M];
     // Time `calls` calls of candidate c (after 2 of warm-up), in us per call.
     auto timed = [&](const Candidate& c, int calls, float* us) {
       int st = run(M, c, 2);
@@ -481,9 +487,17 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
       }
     }
     if (rc != HG_OK) break;
-    const Candidate* best = &cand[0];
-    for (const Candidate& c : cand)
-      if (c.us < best->us) best = &c;
+    // The fixed rule's shape stays unless a candidate is faster by at least
+    // kMargin: differences below that are within run-to-run noise.
+    const Candidate* fastest = &cand[0];
+    const Candidate* rule = nullptr;
+    for (const Candidate& c : cand) {
+      if (c.us < fastest->us) fastest = &c;
+      if (c.s.vpt == fixed.s.vpt && c.s.ctas == fixed.s.ctas && c.s.pref == fixed.s.pref)
+        rule = &c;
+    }
+    const Candidate* best =
+        (rule && fastest->us > rule->us * (1.f - kMargin)) ? rule : fastest;
     h->shape[M] = best->s;
     h->chunks[M] = best->chunks;
   }

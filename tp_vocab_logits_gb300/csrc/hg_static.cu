@@ -111,10 +111,11 @@ extern "C" int hg_gather_static(int tp, int shard_cols, const void* const* shard
   a.M = M;
   a.skip_rank = -1;
 
-  // Launch shape: widest unit, one CTA per unit up to the co-resident
-  // maximum (beyond it the CTAs loop over the units).
+  // Launch shape: the library's fixed rule (elements per lane by tp and M,
+  // one CTA per unit up to the co-resident maximum, beyond which the CTAs
+  // loop over the units).
   hg::LaunchShape s;
-  s.vpt = tp <= 16 ? 4 : 2;
+  s.vpt = hg::default_vpt(tp, M);
   a.chunks = (wv + 32 * s.vpt - 1) / (32 * s.vpt);
   const long long units = (long long)M * tp * a.chunks;
   int per_sm = 0;
