@@ -286,15 +286,17 @@ __device__ __forceinline__ void unit_stats(const GatherArgs& a, const UnitPos& p
   }
 }
 
-// Warp 0 of CTA 0, once its own units are done: poll every row's cells
-// until all have arrived (bounded), fold them, re-arm them and write the [M]
-// statistics. Only warps 0 write cells, so neither a CTA barrier nor any
-// atomic is involved: the cells carry their own arrival, as mailbox words do.
-__device__ __forceinline__ void finish_stats(const GatherArgs& a) {
+// Warp 0 of CTA g, once its own units are done: for rows g, g + G, ..., poll
+// the row's cells until all have arrived (bounded), fold them, re-arm them and
+// write the row's statistics. Rows are reduced by different CTAs in parallel.
+// Only warps 0 write cells, and a reducer waits on cells that consumers write
+// without ever waiting on a reducer, so neither a CTA barrier nor any atomic is
+// involved: the cells carry their own arrival, as mailbox words do.
+__device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) {
   const int lane = (int)threadIdx.x & 31;
   const int per_row = a.tp * a.chunks;  // cells (units) per row
   const uint4 armed = make_uint4(kSentinel, kSentinel, kSentinel, kSentinel);
-  for (int m = 0; m < a.M; ++m) {
+  for (int m = g; m < a.M; m += G) {
     uint4* q = reinterpret_cast<uint4*>(a.partials + (size_t)m * per_row);
     float mx = kNegInf, s = 0.f;
     int arg = 0x7fffffff;
@@ -360,7 +362,7 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a) {
 // VPT: elements per lane per unit. PREF: the next push's shard loads are
 // issued one iteration ahead. MAXT: largest CTA (32 * tp). STATS: warp 0
 // (rank 0's copy of every row) also folds each consumed unit into a
-// statistics cell, and warp 0 of CTA 0 folds the cells of every row.
+// statistics cell, and warp 0 of CTA g folds the cells of rows g, g + G, ...
 template <typename V, int VPT, bool PREF, int MAXT, bool STATS>
 __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
                    "r"(parity ^ 1)
                    : "memory");
   }
-  if (STATS && g == 0 && d == 0) finish_stats(a);  // warp 0 of CTA 0 folds every row's cells
+  if (STATS && d == 0 && g < a.M) finish_stats(a, g, G);  // warp 0 of CTA g: rows g, g + G, ...
 }
 
 __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {

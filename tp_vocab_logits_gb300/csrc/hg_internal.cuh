@@ -25,7 +25,8 @@ constexpr int kStatusWords = 8;
 // Row statistics of one unit's values (max, first argmax, sum of exp(x -
 // max)), 16 bytes. The cells are Lamport cells: armed with the
 // sentinel in every word, written with relaxed stores (a word equal to the
-// sentinel written as zero, as in the gather), polled and re-armed by CTA 0.
+// sentinel written as zero, as in the gather), polled and re-armed by the
+// row's reducer (warp 0 of CTA m mod G for row m).
 struct RowPartial {
   float max;
   int arg;
