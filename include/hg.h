@@ -206,7 +206,9 @@ int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *ele
 
 /*
  * Test hook for failure detection: make rank `rank`'s push skip its rows in
- * every later gather (rank = -1 turns it off). The pollers of the other ranks
+ * every later gather, plain, with statistics or fused (the fused producer
+ * still computes and optionally stores that rank's logits) (rank = -1 turns
+ * it off). The pollers of the other ranks
  * then wait for words that never arrive and give up after the poll bound;
  * hg_sync reports HG_ERR_TIMEOUT. No device fault, trap or endless wait is
  * involved. Errors: HG_ERR_ARG.

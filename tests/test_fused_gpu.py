@@ -121,6 +121,38 @@ def test_fused_config5_full_size_sampled(M):
     h.close()
 
 
+def test_fused_timeout_recovery():
+    """Failure detection in the fused producer without a GPU fault: rank 1's
+    pushes are skipped (host test hook), so the in-kernel pollers of its tiles
+    give up after 20 ms. The grid of 5 CTAs splits the one tail tile into 4
+    parts, so the failure can leave split cells written but unread. hg_sync
+    reports the timeout, later calls are refused until hg_rearm, and after
+    re-arming (mailboxes, split cells, status) the fused call is exact again."""
+    tp, W, K, M = 2, 1024, 576, 2
+    h = hg.hg_create(tp, W, 4, poll_timeout_ns=20_000_000, ctas=5)
+    weight = [synth.weight(9, r, W, K, device="cuda") for r in range(tp)]
+    hid = synth.hidden(9, tp, M, K, device="cuda")
+    hidden = [hid[r] for r in range(tp)]
+    outs = [torch.empty((M, tp * W), dtype=torch.int16, device="cuda") for _ in range(tp)]
+    hg.hg_debug_skip_push(h, 1)
+    hg.hg_gather_fused(h, hidden, weight, outs, M)
+    with pytest.raises(hg.HGError) as e:
+        hg.hg_sync(h)
+    assert e.value.status == hg.HG_ERR_TIMEOUT
+    with pytest.raises(hg.HGError) as e:
+        hg.hg_gather_fused(h, hidden, weight, outs, M)
+    assert e.value.status == hg.HG_ERR_STATE
+    hg.hg_debug_skip_push(h, -1)
+    hg.hg_rearm(h)
+    assert hg.hg_parity(h) == 0
+    assert_mailboxes_armed(h, hg)
+    for call in range(3):
+        outs2, logits = fused_call(h, hidden, weight, M)
+        unfused_equal(outs2, logits, M)
+        assert_mailboxes_armed(h, hg)
+    h.close()
+
+
 def test_fused_rejections():
     tp, W, K = 2, 256, 128
     h = hg.hg_create(tp, W, 17, rows=[1, 2, 17])

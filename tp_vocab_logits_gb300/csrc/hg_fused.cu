@@ -543,8 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
               if (lg) lg[(size_t)m * (a.W / 2) + wcol] = word;
               const uint32_t y = word == kSentinel ? kSentAs : word;
               const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + wcol;
-              for (int d = 0; d < a.tp; ++d)
-                st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off, y);
+              if (r != a.skip_rank)
+                for (int d = 0; d < a.tp; ++d)
+                  st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off, y);
             }
           }
         }
@@ -670,6 +671,7 @@ cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   a.parity_words = l.parity_words;
   a.parity_entries = l.parity_entries;
   a.parity_stride_words = l.parity_stride_words;
+  a.skip_rank = l.skip_rank;
   a.tp = l.tp;
   a.W = l.W;
   a.K = l.K;

@@ -129,6 +129,7 @@ struct FusedArgs {
   int tail;
   int split;
   uint32_t* split_cells;
+  int skip_rank;  // test hook: rank whose mailbox pushes are skipped (-1: none)
 };
 
 // Armed word of a split cell, and the word a partial with that bit pattern
@@ -156,6 +157,7 @@ struct FusedLaunch {
   uint32_t* split_cells = nullptr;  // armed split cells (nullptr: tail tiles are not split)
   size_t split_cell_count = 0;      // cells available (each kSplitCellWords words)
   int max_ctas = 0;                 // cap on the grid (0: one CTA per SM)
+  int skip_rank = -1;               // test hook: rank whose pushes are skipped
 };
 
 // Limits of the fused path: TP, rows, K granularity, W granularity.

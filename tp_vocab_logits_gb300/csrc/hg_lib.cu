@@ -683,6 +683,7 @@ int hg_gather_fused(hg_handle* h, const void* const* hidden_ptrs, const void* co
   l.split_cells = h->split_cells;
   l.split_cell_count = h->split_cell_count;
   l.max_ctas = h->max_ctas;
+  l.skip_rank = h->skip_rank;
   if (hg::fused::fused_launch(l, stream, h->sms) != cudaSuccess) return HG_ERR_CUDA;
   if (!h->device_parity) h->parity ^= 1;
   return HG_OK;
