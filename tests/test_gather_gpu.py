@@ -112,6 +112,13 @@ def test_launch_shapes_vs_oracle(vpt, ctas, pref, coop):
     h.close()
 
 
+@pytest.mark.parametrize("vpt,ctas,pref", [(3, 0, 0), (5, 0, 0), (6, 2, 1), (5, 3, 1), (1, 0, 0)])
+def test_word_path_shapes_vs_oracle(vpt, ctas, pref):
+    """4-byte word path (W % 8 != 0: 499 words per rank-row, ragged for every
+    unit size) with forced elements per lane, grids and prefetch."""
+    run_sequence(3, 998, 4, [4, 1, 3, 2], elems_per_lane=vpt, ctas=ctas, prefetch=pref)
+
+
 def test_multi_wave_decode_width_vs_oracle():
     """TP8, V=163840, M=64: more units than co-resident CTAs, so every CTA loops
     over units; three calls (both parities) against the oracle word for word."""
