@@ -17,7 +17,7 @@ Prints one JSON line (rank 0). Besides the step metric it carries:
   cpu_baseline the CPU oracle on a bounded sample of the step workload
   clocks       SM clocks sampled by nvidia-smi around the timed region
 
---impl reference times the CPU oracle (the reference arm of this build).
+--impl reference times the CPU oracle on the same workload (the reference arm).
 --sweep prints one line per point of the bandwidth sweep instead.
 Multi-GPU: replicas only (one independent gather per GPU; no collective on
 the data path); value = total calls / max-over-ranks time.

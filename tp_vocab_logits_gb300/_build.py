@@ -2,7 +2,7 @@
 
 Each .cu file under csrc/ is compiled by nvcc in parallel, then linked into
 tp_vocab_logits_gb300/libhg.so (static CUDA runtime, so the library needs
-nothing beyond the driver at run time). ptxas resource usage (registers,
+nothing beyond the CUDA driver at run time). ptxas resource usage (registers,
 spills, shared memory) of the last build is kept in _build/ptxas.log.
 
 Alongside, csrc/hg_pycall.c is compiled with the host C compiler into the
