@@ -149,13 +149,14 @@ int hg_destroy(hg_handle *h);
  * outputs; the library owns the mailboxes.
  *
  * Co-residency: the kernel's CTAs wait on one another's pushes, so its whole
- * grid must be resident at once. The grid is sized for an otherwise idle
- * GPU. Kernels that run concurrently on other streams and hold SM resources
- * can keep part of the grid from starting; a multi-iteration call then waits
- * until its poll bound and reports HG_ERR_TIMEOUT at hg_sync. Issue other
- * work on the same stream, or create the handle with hg_options.cooperative
- * = 1, where the runtime itself guarantees co-residency (at the cost of the
- * launch overlap). Errors, all before any device work
+ * grid must become resident. The grid is sized for an otherwise idle GPU.
+ * Kernels running concurrently on other streams can hold SM resources and
+ * keep part of the grid from starting until they release them; the call is
+ * delayed that long, and if that exceeds the poll bound (for example a
+ * persistent kernel on another stream) it reports HG_ERR_TIMEOUT at hg_sync.
+ * Issue such work on the same stream, or create the handle with
+ * hg_options.cooperative = 1, where the runtime itself guarantees
+ * co-residency (at the cost of the launch overlap). Errors, all before any device work
  * and with no parity flip: HG_ERR_ARG (NULL handle or pointer, misaligned
  * pointer), HG_ERR_ROWS (M not served), HG_ERR_CAPTURE (stream capturing,
  * unless the handle has device_parity), HG_ERR_CUDA (launch failed; parity
