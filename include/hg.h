@@ -153,7 +153,9 @@ int hg_destroy(hg_handle *h);
  * Kernels running concurrently on other streams can hold SM resources and
  * keep part of the grid from starting until they release them; the call is
  * delayed that long, and if that exceeds the poll bound (for example a
- * persistent kernel on another stream) it reports HG_ERR_TIMEOUT at hg_sync.
+ * persistent kernel on another stream, including another gather: two gathers
+ * on different streams can each hold the slots the other needs) it reports
+ * HG_ERR_TIMEOUT at hg_sync.
  * Issue such work on the same stream, or create the handle with
  * hg_options.cooperative = 1, where the runtime itself guarantees
  * co-residency (at the cost of the launch overlap). Errors, all before any device work
