@@ -91,7 +91,8 @@ typedef struct hg_options {
                                per lane, CTAs, prefetch) of every served row
                                count on the device and keeps the fastest
                                (the fixed rule's shape unless another is
-                               faster by at least 3 %). The
+                               faster by at least 3 %, in the sweep and again
+                               head to head). The
                                candidates honour the fields above that are
                                set. The timed calls rotate over inputs and
                                outputs in a zero-filled pool of max(256 MB,

@@ -7,6 +7,7 @@
 // test); otherwise the call uses the current parity, flips it, and launches
 // one kernel.
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -413,6 +414,7 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
   constexpr float kBlockUs = 300.f;
   constexpr int kRounds = 3;
   constexpr float kMargin = 0.03f;
+  constexpr int kConfirm = 4;  // even: the median is the mean of the middle two
   const size_t V = (size_t)h->tp * h->W;
   // One set: tp shards [M][W], then tp outputs [M][V], each 16-byte aligned.
   auto set_bytes = [&](int M) { return (size_t)h->tp * M * (h->W + V) * 2; };
@@ -498,6 +500,22 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
     }
     const Candidate* best =
         (rule && fastest->us > rule->us * (1.f - kMargin)) ? rule : fastest;
+    if (rule && best != rule) {
+      // Confirm head to head: kConfirm alternating blocks of the rule's shape
+      // and the challenger; the challenger's median must beat the rule's by
+      // kMargin, else the rule's shape stays.
+      float tr[kConfirm], tc[kConfirm];
+      for (int k = 0; k < kConfirm && rc == HG_OK; ++k) {
+        rc = timed(*rule, block, &tr[k]);
+        if (rc == HG_OK) rc = timed(*best, block, &tc[k]);
+      }
+      if (rc != HG_OK) break;
+      std::sort(tr, tr + kConfirm);
+      std::sort(tc, tc + kConfirm);
+      const float mr = 0.5f * (tr[kConfirm / 2 - 1] + tr[kConfirm / 2]);
+      const float mc = 0.5f * (tc[kConfirm / 2 - 1] + tc[kConfirm / 2]);
+      if (mc > mr * (1.f - kMargin)) best = rule;
+    }
     h->shape[M] = best->s;
     h->chunks[M] = best->chunks;
   }
