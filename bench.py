@@ -478,6 +478,23 @@ def run_ours(args):
                 raise SystemExit(f"bench: e2e output wrong (set {s_}, rank {d})")
     del e2e_calls, host_out
 
+    # the same with one copy of the result read back: rank 0's output in pinned
+    # host memory, ranks 1..TP-1 on the device (every rank's output is the same)
+    host_out0 = torch.empty((nsets, M_STEP, V), dtype=torch.int16).pin_memory()
+    dev_rest = torch.empty((TP - 1, M_STEP, V), dtype=torch.int16, device=device)
+    one_calls = [hg.GatherCall(h, [host_in[s_, r] for r in range(TP)],
+                               [host_out0[s_]] + [dev_rest[d] for d in range(TP - 1)], M_STEP)
+                 for s_ in range(nsets)]
+    one_ms = time_calls(torch, one_calls, args.steps, args.warmup, stream, "timed_e2e_one")
+    hg.hg_sync(h)
+    for s_ in range(nsets):
+        want = torch.cat([host_in[s_, r].view(torch.int32) for r in range(TP)], dim=1)
+        want = torch.where(want == -(1 << 31), torch.zeros_like(want), want)
+        if not torch.equal(host_out0[s_].view(torch.int32), want):
+            raise SystemExit(f"bench: e2e (one copy) output wrong (set {s_})")
+    one_us = round(one_ms * 1000.0 / args.steps, 3)
+    del one_calls, host_out0, dev_rest
+
     # the same with staging copies: H2D of the shards, gather, D2H of the outputs
     dev_in = torch.empty((TP, M_STEP, W), dtype=torch.int16, device=device)
     dev_out = torch.empty((TP, M_STEP, V), dtype=torch.int16, device=device)
@@ -596,7 +613,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": TP * M_STEP * V * 2,
                 "path": "hg_gather_host: pinned host shards read and pinned host outputs "
                         "written by the gather kernel itself over the host-device link",
-                "staged_copies_us_per_call": staged_us},
+                "staged_copies_us_per_call": staged_us,
+                "one_result_copy_to_host_us_per_call": one_us,
+                "one_result_copy_d2h_bytes_per_step": M_STEP * V * 2},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                      "traffic": traffic,
