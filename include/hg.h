@@ -88,8 +88,9 @@ typedef struct hg_options {
                                host learns the parity only at hg_sync */
   int autotune;             /* 0 (default): launch shapes from a fixed rule; 1:
                                hg_create_ex times candidate shapes (elements
-                               per lane, CTAs, prefetch) of every served row
-                               count on the device and keeps the fastest
+                               per lane, CTAs, prefetch) of hg_gather for every
+                               served row count on the device and keeps the
+                               fastest (hg_gather_stats keeps the fixed rule)
                                (the fixed rule's shape unless another is
                                faster by at least 3 %, in the sweep and again
                                head to head). The

@@ -457,7 +457,8 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
     if (!h->served[M]) continue;
     std::vector<Candidate> cand;
     rc = tune_candidates(h, M, opt, &cand);
-    if (rc != HG_OK || cand.empty()) break;
+    if (rc != HG_OK) break;
+    if (cand.empty()) continue;  // nothing to time (e.g. prefetch forced, one wave): fixed rule
     Candidate fixed;  // the fixed rule's shape, as planned before tuning
     fixed.s = h->shape[M];
     fixed.chunks = h->chunks[M];
