@@ -36,16 +36,19 @@
 // other part writes its partial [128 x M] into a split cell, and the owner
 // polls the cell, adds it, re-arms the cell, rounds and pushes. A split cell
 // is a Lamport cell like a mailbox row: armed with 0xffffffff in every word
-// (a NaN that the accumulation never produces; a partial with that bit
-// pattern is written as the NaN 0x7fffffff instead), written with relaxed
-// stores, polled until no armed word is left, and re-armed by its reader.
+// (a NaN; a partial with that bit pattern is written as the NaN 0x7fffffff
+// instead, the same value to the addition), written with relaxed stores,
+// polled until no armed word is left, and re-armed by its reader.
 //
-// Gather. After its own tiles, CTA g polls the tiles that CTA g+1 (mod G)
-// pushed (its whole tiles and the tail tile it owns) in every rank's mailbox,
-// copies them to the outputs and re-arms, as the gather kernel does. Every
-// wait in this kernel (mbarriers and polls) is bounded by %globaltimer; on
-// expiry the kernel records the error in the status block, lets its
-// in-flight copies and MMAs drain, frees its tensor memory and returns.
+// Gather. CTA g consumes the tiles that CTA g+1 (mod G) pushed (its whole
+// tiles and the tail tile it owns): it polls them in every rank's mailbox,
+// copies them to the outputs and re-arms, as the gather kernel does. The
+// epilogue warps do this one item behind their own pushes, so the gather
+// overlaps the weight stream; the last one or two tiles are consumed by all
+// threads after the CTA's own tiles. Every wait in this kernel (mbarriers and
+// polls) is bounded by %globaltimer; on expiry the kernel records the error
+// in the status block, lets its in-flight copies and MMAs drain, frees its
+// tensor memory and returns.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
