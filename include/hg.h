@@ -249,10 +249,17 @@ int hg_debug_skip_push(hg_handle *h, int rank);
  *   M            rows: served by the handle and <= 16
  *   K            hidden size: a positive multiple of 64
  *
- * Requires tp <= 16 and W a multiple of 128. Errors, before any device work
- * and with no parity flip: HG_ERR_ARG, HG_ERR_ROWS, HG_ERR_CAPTURE,
- * HG_ERR_STATE, HG_ERR_CUDA (launch or tensor-map encoding failed). A wait
- * that times out is reported by hg_sync, as for hg_gather.
+ * Requires tp <= 16 and W a multiple of 128. One CTA per SM (a cooperative
+ * launch; hg_options.ctas caps the grid). When the vocab tiles do not divide
+ * evenly over the CTAs, the last tiles are split along K over several CTAs,
+ * whose fp32 partials meet in the handle's split cells; the sum of the parts
+ * may round differently from one accumulation over K (fp32), which the
+ * logits tolerance covers, and the gathered outputs are always exactly the
+ * gather of the returned logits. Errors, before any device work and with no
+ * parity flip: HG_ERR_ARG, HG_ERR_ROWS, HG_ERR_CAPTURE, HG_ERR_STATE,
+ * HG_ERR_CUDA (launch or tensor-map encoding failed). A wait that times out is
+ * reported by hg_sync, as for hg_gather; hg_rearm also re-arms the split
+ * cells.
  */
 int hg_gather_fused(hg_handle *h, const void *const *hidden_ptrs, const void *const *weight_ptrs,
                     void *const *logits_ptrs, void *const *out_ptrs, int M, int K,
