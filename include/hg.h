@@ -196,9 +196,10 @@ int hg_gather_host(hg_handle *h, const void *const *shard_ptrs, void *const *out
  * or HG_ERR_CUDA. */
 int hg_sync(hg_handle *h, hg_stream_t stream);
 
-/* Recovery after an error (the mailbox is the only state besides the parity):
- * refill every mailbox word of both parities with the sentinel, clear the
- * status word and set the parity to 0, on `stream`, asynchronously. */
+/* Recovery after an error: refill every mailbox word of both parities with
+ * the sentinel, re-arm the statistics cells and the fused producer's split
+ * cells, clear the status words and set the parity to 0 (host and device
+ * copies), on `stream`, asynchronously. */
 int hg_rearm(hg_handle *h, hg_stream_t stream);
 
 /* Parity the next hg_gather uses (0 or 1; starts at 0, flips per served call
