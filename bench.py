@@ -753,6 +753,42 @@ def run_sweep(args):
     return 0
 
 
+def run_stats_only(args):
+    """hg_gather_stats on the step workload (TP8, V=163840, cap 8, M rows),
+    one JSON line per M: us/call, checked against the plain gather's outputs."""
+    import ctypes
+
+    import torch
+
+    from tp_vocab_logits_gb300 import _build, hg, synth
+    _build.build()
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    lib = hg.load()
+    for M in [int(x) for x in args.stats_ms.split(",")]:
+        n = sets_for(TP, W, M)
+        h, sh, ou, calls = make_workload(torch, hg, synth, TP, W, CAP, M, n, device, rows=[M])
+        st = hg.new_row_stats(M)
+        arrs = [((ctypes.c_void_p * TP)(*[sh[s_, r].data_ptr() for r in range(TP)]),
+                 (ctypes.c_void_p * TP)(*[ou[s_, d].data_ptr() for d in range(TP)]))
+                for s_ in range(n)]
+        sp = stream.cuda_stream
+        fns = [lambda a_=a_: lib.hg_gather_stats(h.ptr, a_[0], a_[1], M, st.data_ptr(), sp)
+               for a_ in arrs]
+        fns[0]()
+        hg.hg_sync(h)
+        check_concat(torch, sh[0], ou[0], TP, f"stats M={M}")
+        t = time_calls(torch, fns, args.calls, 5, stream, "timed_stats")
+        hg.hg_sync(h)
+        print(json.dumps({"stats": "hg_gather_stats", "tp": TP, "shard_cols": W, "M": M,
+                          "calls": args.calls, "us_per_call": round(t * 1000.0 / args.calls, 3)}),
+              flush=True)
+        h.close()
+        del sh, ou, calls, fns
+    return 0
+
+
 def run_fused_only(args):
     import torch
 
@@ -783,6 +819,9 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true",
                     help="fused LM-head producer only (TP8, K=7168, V=163840), one line per M")
     ap.add_argument("--fused-ms", default="1,4,8")
+    ap.add_argument("--stats", action="store_true",
+                    help="hg_gather_stats only (TP8, V=163840), one line per M")
+    ap.add_argument("--stats-ms", default="1,4,8")
     ap.add_argument("--fused-w", type=int, default=20480, help="fused: shard columns per rank")
     ap.add_argument("--tps", default="2,4,8,16")
     ap.add_argument("--widths", default="4096,8192,20480,65536")
@@ -806,6 +845,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.fused:
         return run_fused_only(args)
+    if args.stats:
+        return run_stats_only(args)
     return run_ours(args)
 
 
