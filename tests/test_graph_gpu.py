@@ -147,3 +147,37 @@ def test_host_buffers_graph_replay_vs_oracle():
         assert hg.hg_parity(h) == og.parity
     assert_mailboxes_armed(h, hg)
     h.close()
+
+
+def test_stats_graph_replay_vs_oracle():
+    """hg_gather_stats on a device-parity handle (TP8, V=163840, M=4), two
+    calls captured once and replayed twice: outputs and row statistics
+    against the oracle each replay (the statistics cells re-arm themselves)."""
+    tp, W, cap, M = 8, 20480, 4, 4
+    h = hg.hg_create(tp, W, cap, device_parity=True)
+    og = oracle.Gather(tp, W, cap)
+    sets = [synth.shards(41, tp, M, W, scale=3.0, sent_frac=0.01, set_index=i)
+            .numpy().view(np.uint16) for i in range(2)]
+    dev = [to_dev(b) for b in sets]
+    outs = [empty_outs(tp, M, tp * W) for _ in range(2)]
+    stats = [hg.new_row_stats(M) for _ in range(2)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(2):
+            hg.hg_gather_stats(h, dev[i], outs[i], stats[i], M, stream=s)
+    for replay in range(2):
+        wants = [og.call(sets[i]) for i in range(2)]
+        g.replay()
+        torch.cuda.synchronize()
+        hg.hg_sync(h)
+        for i in range(2):
+            np.testing.assert_array_equal(from_dev(outs[i]), wants[i])
+            got = {k: v.cpu().numpy() for k, v in hg.unpack_row_stats(stats[i]).items()}
+            for m in range(M):
+                mx, arg, se = oracle.row_stats(wants[i][0][m])
+                assert got["max_logit"][m] == mx and got["argmax"][m] == arg
+                assert abs(got["sum_exp"][m] - se) <= 1e-4 * se
+    assert_mailboxes_armed(h, hg)
+    h.close()
