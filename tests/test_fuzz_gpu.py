@@ -64,3 +64,44 @@ def test_random_configuration_vs_oracle(case):
         assert hg.hg_parity(h) == og.parity
     assert_mailboxes_armed(h, hg)
     h.close()
+
+
+def draw_fused(case: int) -> dict:
+    rng = random.Random(5000 + case)
+    return {"tp": rng.randint(1, 8), "W": 128 * rng.randint(1, 12), "K": 64 * rng.randint(1, 12),
+            "M": rng.randint(1, 16), "ctas": rng.choice([0, 2, 3, 5, 7, 11, 13])}
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_random_fused_configuration(case):
+    """The fused LM head + gather on seeded random shapes and grids (tail
+    splits of 2..4 parts, unsplit tails, one wave): logits within
+    2e-2 + 1e-2 * |ref| of the oracle's float64 product, and the gathered
+    outputs bit-exact to hg_gather of those logits."""
+    import torch
+    c = draw_fused(case)
+    tp, W, K, M = c["tp"], c["W"], c["K"], c["M"]
+    h = hg.hg_create(tp, W, 16, ctas=c["ctas"])
+    weight_cpu = [synth.weight(60 + case, r, W, K) for r in range(tp)]
+    hid_cpu = synth.hidden(60 + case, tp, M, K)
+    weight = [w.cuda() for w in weight_cpu]
+    hidden = [hid_cpu[r].cuda() for r in range(tp)]
+    outs = [torch.full((M, tp * W), 0x2222, dtype=torch.int16, device="cuda") for _ in range(tp)]
+    logits = [torch.full((M, W), 0x3333, dtype=torch.int16, device="cuda") for _ in range(tp)]
+    hg.hg_gather_fused(h, hidden, weight, outs, M, logits=logits)
+    hg.hg_sync(h)
+    for r in range(tp):
+        ref = oracle.lm_head_f64(hid_cpu[r].numpy().view(np.uint16),
+                                 weight_cpu[r].numpy().view(np.uint16))
+        got = torch.from_numpy(logits[r].cpu().numpy()).view(torch.bfloat16).double().numpy()
+        bad = np.abs(got - ref) > 2e-2 + 1e-2 * np.abs(ref)
+        assert not bad.any(), f"{c}: rank {r}: {int(bad.sum())} logits outside tolerance"
+    h2 = hg.hg_create(tp, W, 16)
+    ref_out = [torch.empty_like(o) for o in outs]
+    hg.hg_gather(h2, logits, ref_out, M)
+    hg.hg_sync(h2)
+    h2.close()
+    for d in range(tp):
+        assert torch.equal(outs[d], ref_out[d]), f"{c}: rank {d} differs from the gather"
+    assert_mailboxes_armed(h, hg)
+    h.close()
