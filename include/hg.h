@@ -98,8 +98,9 @@ typedef struct hg_options {
                                set. The timed calls rotate over inputs and
                                outputs in a zero-filled pool of max(256 MB,
                                tp * M * (W + tp * W) * 2 bytes) that is freed
-                               before returning; row counts whose one set
-                               would exceed 1 GB keep the fixed rule. It costs
+                               before returning; row counts above 16, and those
+                               whose one set would exceed 1 GB, keep the fixed
+                               rule. It costs
                                tens of milliseconds per served row count at the
                                decode sizes and changes no result, only speed */
 } hg_options;

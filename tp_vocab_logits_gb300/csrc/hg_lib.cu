@@ -411,6 +411,9 @@ int tune_candidates(hg_handle* h, int M, const hg_options* opt, std::vector<Cand
 int autotune_shapes(hg_handle* h, const hg_options* opt) {
   constexpr size_t kSetLimit = 1ull << 30;
   constexpr size_t kPoolBytes = 256ull << 20;
+  // Row counts above this keep the fixed rule: tuning pays at decode sizes,
+  // and from M = 32 on the fixed rule runs at the memory roofline.
+  constexpr int kMaxTunedRows = 16;
   constexpr float kBlockUs = 300.f;
   constexpr int kRounds = 3;
   constexpr float kMargin = 0.03f;
@@ -419,7 +422,7 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
   // One set: tp shards [M][W], then tp outputs [M][V], each 16-byte aligned.
   auto set_bytes = [&](int M) { return (size_t)h->tp * M * (h->W + V) * 2; };
   int maxM = 0;
-  for (int M = 1; M <= h->cap; ++M)
+  for (int M = 1; M <= h->cap && M <= kMaxTunedRows; ++M)
     if (h->served[M] && set_bytes(M) <= kSetLimit) maxM = M;
   if (maxM == 0) return HG_OK;
   const size_t pool_bytes = set_bytes(maxM) > kPoolBytes ? set_bytes(maxM) : kPoolBytes;
