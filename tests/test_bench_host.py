@@ -1,0 +1,65 @@
+"""Host-side logic of bench.py, without a GPU: the algorithmic-byte formula,
+the number of rotating input sets, the output check, the replica arithmetic
+and the lookup of the profiled DRAM traffic."""
+
+import hashlib
+import json
+import os
+
+import pytest
+import torch
+
+import bench
+
+S = -(1 << 31)  # the sentinel word as a signed int32
+
+
+def test_algorithmic_bytes_formula():
+    # M * V * 2 * (1 + 4 * TP): shard read, then push, poll, output, re-arm per rank
+    assert bench.algorithmic_bytes(8, 20480, 1) == 10_813_440
+    assert bench.algorithmic_bytes(8, 20480, 64) == 64 * 10_813_440
+    assert bench.algorithmic_bytes(2, 4, 1) == 1 * 8 * 2 * 9
+
+
+def test_sets_exceed_twice_the_l2():
+    for tp, W, M in [(8, 20480, 1), (8, 20480, 8), (2, 4096, 1), (16, 65536, 256)]:
+        n = bench.sets_for(tp, W, M)
+        per = M * tp * W * 2 * (1 + tp)
+        assert n >= 3
+        assert n * per >= 2 * bench.L2_BYTES
+
+
+def test_check_concat_accepts_rewritten_concat_and_rejects_errors():
+    tp, M, W = 3, 2, 8
+    g = torch.Generator().manual_seed(0)
+    shards = torch.randint(-30000, 30000, (tp, M, W), dtype=torch.int16, generator=g)
+    shards.view(torch.int32)[0, 0, 1] = S  # a sentinel word in rank 0
+    want = torch.cat([shards[r].view(torch.int32) for r in range(tp)], dim=1)
+    want = torch.where(want == S, torch.zeros_like(want), want)
+    outs = torch.stack([want.view(torch.int16)] * tp)
+    bench.check_concat(torch, shards, outs, tp, "ok")
+    outs[2].view(torch.int32)[1, 3] ^= 1
+    with pytest.raises(SystemExit):
+        bench.check_concat(torch, shards, outs, tp, "corrupted")
+    outs = torch.stack([torch.cat([shards[r].view(torch.int32) for r in range(tp)], dim=1)
+                        .view(torch.int16)] * tp)  # sentinel not rewritten
+    with pytest.raises(SystemExit):
+        bench.check_concat(torch, shards, outs, tp, "no rewrite")
+
+
+def test_replica_arithmetic_single_process():
+    ms_max, us = bench.replica_us_per_call(None, 4.0, 1000, 1, None)
+    assert ms_max == 4.0 and us == pytest.approx(4.0)
+
+
+def test_traffic_lookup_follows_the_kernel_hash():
+    with open(bench.TRAFFIC_FILE) as f:
+        d = json.load(f)
+    with open(bench.KERNEL_SRC, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    got = bench.traffic_from_profile("tp8_w20480_m1")
+    if d["kernel_sha256_16"] == h:
+        assert got == d["per_launch_dram_bytes"]["tp8_w20480_m1"]
+    else:
+        assert got is None  # counters of another kernel source are not reported
+    assert bench.traffic_from_profile("no_such_workload") is None
