@@ -1,7 +1,7 @@
 """CPU oracle of the vocab-parallel logits gather (ctypes wrapper).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
-CPU-baseline leg of ``bench.py`` may use this package; the library under
+CPU-baseline leg and reference arm of ``bench.py`` may use this package; the library under
 ``tp_vocab_logits_gb300`` never imports it and shares no code with it.
 
 The arithmetic lives in ``hg_oracle.cpp`` (plain C++, compiled with g++); this

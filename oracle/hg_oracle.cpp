@@ -3,7 +3,7 @@
 //
 // TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct
 // statement of what the GPU path computes. Only the tests, the smoke check and
-// the CPU-baseline leg of the benchmark may load it. It shares no code, header,
+// the benchmark's CPU-baseline leg and reference arm may load it. It shares no code, header,
 // constant or helper with the CUDA library, and the library never calls it.
 //
 // Source of the definition: the vLLM API page
