@@ -470,7 +470,8 @@ def run_ours(args):
                  for s_ in range(nsets)]
     e2e_ms = time_calls(torch, e2e_calls, args.steps, args.warmup, stream, "timed_e2e")
     hg.hg_sync(h)
-    for s_ in range(nsets):
+    used = min(nsets, max(args.steps, args.warmup))  # sets the calls above wrote
+    for s_ in range(used):
         want = torch.cat([host_in[s_, r].view(torch.int32) for r in range(TP)], dim=1)
         want = torch.where(want == -(1 << 31), torch.zeros_like(want), want)
         for d in range(TP):
@@ -487,7 +488,7 @@ def run_ours(args):
                  for s_ in range(nsets)]
     one_ms = time_calls(torch, one_calls, args.steps, args.warmup, stream, "timed_e2e_one")
     hg.hg_sync(h)
-    for s_ in range(nsets):
+    for s_ in range(used):
         want = torch.cat([host_in[s_, r].view(torch.int32) for r in range(TP)], dim=1)
         want = torch.where(want == -(1 << 31), torch.zeros_like(want), want)
         if not torch.equal(host_out0[s_].view(torch.int32), want):
