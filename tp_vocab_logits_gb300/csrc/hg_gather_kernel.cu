@@ -400,8 +400,9 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   int parity = 0;
   if (a.parity_words) parity = ld_relaxed_s32(a.parity_words + reader);
   // Let the next kernel on the stream start launching (it waits for this one
-  // to complete before it touches memory).
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // to complete before it touches memory): here, or once this warp's work is
+  // done (late_trigger).
+  if (!a.late_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // One load per warp of one address: every lane sees the same value.
   if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
 
@@ -460,6 +461,7 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
       if (STATS && d == 0) unit_stats<V, VPT>(a, p, uc, res);
     }
   }
+  if (a.late_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (a.parity_words) {
     // Flip this warp's share of the parity copies: copies reader + k * G * tp,
     // so that every copy flips exactly once per call whatever the grid size.
@@ -526,6 +528,8 @@ cudaError_t launch_gather(const GatherArgs& a, const LaunchShape& s, bool vec16,
                           cudaStream_t stream, bool cooperative) {
   const void* k = kernel_for(s, vec16, a.tp);
   if (!k) return cudaErrorInvalidValue;
+  GatherArgs args = a;
+  args.late_trigger = s.late ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)s.ctas);
   cfg.blockDim = dim3((unsigned)(32 * a.tp));
@@ -541,8 +545,8 @@ cudaError_t launch_gather(const GatherArgs& a, const LaunchShape& s, bool vec16,
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {const_cast<GatherArgs*>(&a)};
-  return cudaLaunchKernelExC(&cfg, k, args);
+  void* kargs[] = {&args};
+  return cudaLaunchKernelExC(&cfg, k, kargs);
 }
 
 cudaError_t launch_fill_u32(uint32_t* p, size_t n, uint32_t v, cudaStream_t stream) {

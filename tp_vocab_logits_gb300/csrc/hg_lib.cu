@@ -117,6 +117,7 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchS
   long long G = want < maxg ? want : maxg;
   if (G < 1) G = 1;
   s.ctas = (int)G;
+  s.late = hg::trigger_late(G, units, maxg);
   *out = s;
   *chunks_out = chunks;
   return HG_OK;
@@ -389,6 +390,7 @@ int tune_candidates(hg_handle* h, int M, const hg_options* opt, std::vector<Cand
         const long long iters = (units + g - 1) / g;
         if (pref && iters < 2) continue;
         c.s.ctas = (int)g;
+        c.s.late = hg::trigger_late(g, units, maxg);
         out->push_back(c);
       }
     }

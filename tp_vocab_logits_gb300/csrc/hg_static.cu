@@ -122,6 +122,7 @@ extern "C" int hg_gather_static(int tp, int shard_cols, const void* const* shard
   if (hg::gather_occupancy(s, vec16, tp, &per_sm) != cudaSuccess || per_sm < 1) return HG_ERR_CUDA;
   const long long maxg = (long long)per_sm * ds.sms;
   s.ctas = (int)(units < maxg ? units : maxg);
+  s.late = hg::trigger_late(s.ctas, units, maxg);
 
   // The array keeps the last call's contents: clear the status words and arm
   // this call's mailbox region, then gather, all in stream order.
