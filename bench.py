@@ -769,7 +769,8 @@ def run_stats_only(args):
     lib = hg.load()
     for M in [int(x) for x in args.stats_ms.split(",")]:
         n = sets_for(TP, W, M)
-        h, sh, ou, calls = make_workload(torch, hg, synth, TP, W, CAP, M, n, device, rows=[M])
+        kw = {"elems_per_lane": args.vpt} if args.vpt else {}
+        h, sh, ou, calls = make_workload(torch, hg, synth, TP, W, CAP, M, n, device, rows=[M], **kw)
         st = hg.new_row_stats(M)
         arrs = [((ctypes.c_void_p * TP)(*[sh[s_, r].data_ptr() for r in range(TP)]),
                  (ctypes.c_void_p * TP)(*[ou[s_, d].data_ptr() for d in range(TP)]))
@@ -783,7 +784,8 @@ def run_stats_only(args):
         t = time_calls(torch, fns, args.calls, 5, stream, "timed_stats")
         hg.hg_sync(h)
         print(json.dumps({"stats": "hg_gather_stats", "tp": TP, "shard_cols": W, "M": M,
-                          "calls": args.calls, "us_per_call": round(t * 1000.0 / args.calls, 3)}),
+                          "calls": args.calls, "us_per_call": round(t * 1000.0 / args.calls, 3),
+                          "elems_per_lane": args.vpt or None}),
               flush=True)
         h.close()
         del sh, ou, calls, fns
@@ -829,7 +831,7 @@ def main(argv=None):
     ap.add_argument("--ms", default="1,8,32,64,128,256")
     ap.add_argument("--calls", type=int, default=200)
     ap.add_argument("--max-gb", type=float, default=120.0)
-    ap.add_argument("--vpt", type=int, default=0, help="sweep: force elements per lane")
+    ap.add_argument("--vpt", type=int, default=0, help="sweep and --stats: force elements per lane")
     ap.add_argument("--ctas", type=int, default=0, help="sweep: force the CTA count")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="sweep: 1 shard prefetch on, 2 off (0: chosen per row count)")

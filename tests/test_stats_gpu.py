@@ -84,6 +84,10 @@ def test_stats_ties_and_special_rows():
     (16, 4096, 2, [2], {}),
     (8, 20480, 8, [8, 1], {"device_parity": True}),
     (1, 64, 2, [2, 1], {}),                                # degenerate TP=1
+    (8, 20480, 2, [2, 1], {"elems_per_lane": 1}),          # 640 cells a row: 3 reducer batches
+    (8, 20480, 2, [1, 2], {"elems_per_lane": 4}),          # the VPT 4 kernel at decode sizes
+    (16, 65536, 1, [1], {"elems_per_lane": 5}),            # 6-cell batches, 832 cells: 5 batches
+    (4, 6144, 3, [3], {"elems_per_lane": 6}),
 ])
 def test_stats_shapes(tp, W, cap, Ms, kw):
     h = hg.hg_create(tp, W, cap, **kw)

@@ -205,7 +205,6 @@ __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, con
 // ---- Row statistics (max, first argmax, sum of exp(x - max)) -------------
 
 constexpr float kNegInf = -__builtin_huge_valf();
-constexpr int kCellBatch = 6;  // statistics cells each reducer thread loads at once
 
 // (mx, arg) <- the larger of (mx, arg) and (x, col); ties keep the smaller column.
 __device__ __forceinline__ void max_add(float& mx, int& arg, float x, int col) {
@@ -288,10 +287,13 @@ __device__ __forceinline__ void unit_stats(const GatherArgs& a, const UnitPos& p
 
 // Warp 0 of CTA g, once its own units are done: for rows g, g + G, ..., poll
 // the row's cells until all have arrived (bounded), fold them, re-arm them and
-// write the row's statistics. Rows are reduced by different CTAs in parallel.
+// write the row's statistics. BATCH cells per lane are in flight at once, so a
+// row of up to 32 * BATCH cells costs one wait. Rows are reduced by different
+// CTAs in parallel.
 // Only warps 0 write cells, and a reducer waits on cells that consumers write
 // without ever waiting on a reducer, so neither a CTA barrier nor any atomic is
 // involved: the cells carry their own arrival, as mailbox words do.
+template <int BATCH>
 __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) {
   const int lane = (int)threadIdx.x & 31;
   const int per_row = a.tp * a.chunks;  // cells (units) per row
@@ -301,13 +303,13 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
     float mx = kNegInf, s = 0.f;
     int arg = 0x7fffffff;
     bool gave_up = false;
-    for (int base = lane; base < per_row && !gave_up; base += kCellBatch * 32) {
+    for (int base = lane; base < per_row && !gave_up; base += BATCH * 32) {
       // A batch of cells in flight; the ones still armed are re-loaded
       // together (never one at a time), until all have arrived (bounded).
-      uint4 v[kCellBatch];
+      uint4 v[BATCH];
       unsigned todo = 0;
 #pragma unroll
-      for (int k = 0; k < kCellBatch; ++k) {
+      for (int k = 0; k < BATCH; ++k) {
         if (base + 32 * k < per_row) {
           v[k] = Elem<uint4>::ld_poll(q + base + 32 * k);
           todo |= 1u << k;
@@ -317,7 +319,7 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
       unsigned long long t0 = 0;
       for (;;) {
 #pragma unroll
-        for (int k = 0; k < kCellBatch; ++k)
+        for (int k = 0; k < BATCH; ++k)
           if ((todo >> k & 1) && Elem<uint4>::arrived(v[k])) todo &= ~(1u << k);
         if (!todo) break;
         const unsigned long long now = globaltimer_ns();
@@ -328,32 +330,46 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
           break;
         }
 #pragma unroll
-        for (int k = 0; k < kCellBatch; ++k)
+        for (int k = 0; k < BATCH; ++k)
           if (todo >> k & 1) v[k] = Elem<uint4>::ld_poll(q + base + 32 * k);
       }
       if (gave_up) break;
+      // The batch's max and first argmax, then its sum rescaled to that max:
+      // the exponentials are independent of one another.
+      float bm = kNegInf, bs = 0.f;
+      int ba = 0x7fffffff;
 #pragma unroll
-      for (int k = 0; k < kCellBatch; ++k) {
+      for (int k = 0; k < BATCH; ++k)
+        if (valid >> k & 1) max_add(bm, ba, __uint_as_float(v[k].x), (int)v[k].y);
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
         if (!(valid >> k & 1)) continue;
-        combine_partial(mx, arg, s, __uint_as_float(v[k].x), (int)v[k].y,
-                        __uint_as_float(v[k].z));
+        const float ck = __uint_as_float(v[k].x);
+        if (ck != kNegInf) bs += __uint_as_float(v[k].z) * __expf(ck - bm);
         Elem<uint4>::st_relaxed(q + base + 32 * k, armed);
       }
+      combine_partial(mx, arg, s, bm, ba, bs);
     }
+    // Across the warp in the same two steps: max and first argmax, then the
+    // lanes' sums rescaled to it.
+    float rm = mx;
+    int ra = arg;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const float m2 = __shfl_xor_sync(kFull, mx, off);
-      const int a2 = __shfl_xor_sync(kFull, arg, off);
-      const float s2 = __shfl_xor_sync(kFull, s, off);
-      combine_partial(mx, arg, s, m2, a2, s2);
+      const float m2 = __shfl_xor_sync(kFull, rm, off);
+      const int a2 = __shfl_xor_sync(kFull, ra, off);
+      max_add(rm, ra, m2, a2);
     }
+    float rs = mx != kNegInf ? s * __expf(mx - rm) : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) rs += __shfl_xor_sync(kFull, rs, off);
     if (__any_sync(kFull, gave_up)) return;
     if (lane == 0) {
       hg_row_stats r;
-      r.max_logit = mx;
-      r.argmax = arg;
-      r.sum_exp = s;
-      r.logsumexp = mx + logf(s);
+      r.max_logit = rm;
+      r.argmax = ra;
+      r.sum_exp = rs;
+      r.logsumexp = rm + logf(rs);
       a.stats[m] = r;
     }
   }
@@ -473,7 +489,10 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
                    "r"(parity ^ 1)
                    : "memory");
   }
-  if (STATS && d == 0 && g < a.M) finish_stats(a, g, G);  // warp 0 of CTA g: rows g, g + G, ...
+  // Warp 0 of CTA g: rows g, g + G, ... Eight cells per lane cover a row of
+  // TP8 V=163840 at 3 elements per lane (216 cells) in one wait; wider units
+  // leave fewer cells and fewer free registers.
+  if (STATS && d == 0 && g < a.M) finish_stats<(VPT <= 4 ? 8 : 6)>(a, g, G);
 }
 
 __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {

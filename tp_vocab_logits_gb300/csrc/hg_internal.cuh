@@ -101,6 +101,11 @@ inline int default_vpt(int tp, int M) {
   return (tp <= 8 && M <= 2) ? 3 : 4;
 }
 
+// Elements per lane of the statistics kernel (tp <= 16) for M rows: 3 up to
+// eight rows at tp <= 8, where the smaller units shorten each consumer's fold
+// and the reducer still polls a row's cells in one wait; 4 otherwise.
+inline int stats_vpt(int tp, int M) { return (tp <= 8 && M <= 8) ? 3 : 4; }
+
 // Largest co-resident CTAs per SM of the gather kernel for this shape.
 cudaError_t gather_occupancy(const LaunchShape& s, bool vec16, int tp, int* ctas_per_sm);
 

@@ -101,10 +101,10 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchS
   const int forced_ctas = opt ? opt->ctas : 0;
   hg::LaunchShape s;
   s.stats = stats;
-  // The statistics kernel keeps 4 elements per lane: its final reduction
-  // folds one cell per unit, and fewer, larger units measured faster (TP8,
-  // V=163840, M=1: 6.5 us with 4 per lane, 8.4 us with 3).
-  s.vpt = forced_vpt ? forced_vpt : (stats ? 4 : hg::default_vpt(h->tp, M));
+  // The statistics kernel has its own rule: its reducer polls one cell per
+  // unit (TP8, V=163840: 3 per lane measured 6.1-6.2 us at M=1 and 14.8 us at
+  // M=8, against 6.5 and 15.6 us with 4).
+  s.vpt = forced_vpt ? forced_vpt : (stats ? hg::stats_vpt(h->tp, M) : hg::default_vpt(h->tp, M));
   s.pref = opt && opt->prefetch == 1;
   const int chunks = (h->wv + 32 * s.vpt - 1) / (32 * s.vpt);
   const long long units = (long long)M * h->tp * chunks;
