@@ -4,8 +4,9 @@ Per gathered row: max_logit and argmax must equal the oracle exactly (the max
 of bf16 values is exact in fp32, and both sides resolve ties to the smallest
 column); sum_exp, accumulated in fp32 with the fast exponential, within a
 relative 1e-4 of the oracle's float64 sum (a few ulp per term over per-lane
-runs of at most 32 terms, then pairwise folding); logsumexp within 1e-4
-absolute. The gathered outputs themselves stay bit-exact."""
+runs of at most 48 terms, then runs of at most 8 cells and pairwise
+folding); logsumexp within 1e-4 absolute. The gathered outputs themselves stay
+bit-exact."""
 
 import numpy as np
 import pytest
