@@ -151,6 +151,13 @@ int hg_destroy(hg_handle *h);
  * Uses parity hg_parity(h), then flips it. The caller owns the shards and the
  * outputs; the library owns the mailboxes.
  *
+ * The launch may start while the previous kernel on `stream` still runs (a
+ * programmatic dependent launch). Before it waits for that kernel to
+ * complete, each CTA asks L2 to prefetch the first bytes of shard it will
+ * read (on the vector path). That is a cache hint only: every value the
+ * gather reads is read after the previous kernel has completed, so the
+ * shards may be that kernel's output.
+ *
  * Co-residency: the kernel's CTAs wait on one another's pushes, so its whole
  * grid must become resident. The grid is sized for an otherwise idle GPU.
  * Kernels running concurrently on other streams can hold SM resources and
@@ -182,6 +189,8 @@ int hg_gather(hg_handle *h, const void *const *shard_ptrs, void *const *out_ptrs
  * host-device link (no staging copies), while the mailboxes stay in device
  * memory. Same arguments, contract and errors as hg_gather, plus:
  *
+ *   no L2 prefetch of the shards before the wait (the host may still be
+ *   writing them);
  *   every pointer is checked with cudaPointerGetAttributes and replaced by its
  *   device-side address; pageable host memory, memory of another device and
  *   unknown addresses give HG_ERR_ARG before any device work.

@@ -382,11 +382,6 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
 template <typename V, int VPT, bool PREF, int MAXT, bool STATS>
 __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
-  // Programmatic dependent launch: wait until the previous kernel on the
-  // stream has completed and its memory is visible. Nothing is read or
-  // written before the wait.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
   const int lane = (int)threadIdx.x & 31;
   const int d = (int)threadIdx.x >> 5;  // this warp's rank: mailbox and output
   const int N = a.M * a.tp * a.chunks;  // units
@@ -394,21 +389,40 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   const int g = (int)blockIdx.x;
   const int cons = (g + 1 == G) ? 0 : g + 1;  // the CTA whose pushes we consume
   const int iters = (N + G - 1) / G;
+  // The first push's position needs only the arguments: compute it before
+  // the wait, off the path that starts when the previous kernel completes.
+  UnitPos p0{};
+  const bool push0 = iters > 0 && g < N;
+  if (push0) p0 = unit_pos<VPT>(a, g, lane);
+  // Before the wait, only an L2 prefetch of that unit (16-byte vectors), so
+  // that its DRAM round trip overlaps the previous kernel. It brings no value
+  // into the SM, and every access to device memory goes through L2, so the
+  // loads after the wait still see what the previous kernel writes to the
+  // shards. The unit is contiguous: 32 * VPT vectors from lane 0's first,
+  // fewer in a ragged last chunk.
+  if constexpr (sizeof(V) == 16) {
+    if (a.l2_prefetch && threadIdx.x == 0 && push0 && p0.r != a.skip_rank) {
+      const int n = min(32 * VPT, a.wv - p0.idx);
+      if (n > 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     ::"l"(reinterpret_cast<const V*>(a.shard[p0.r]) + p0.src), "r"(n * 16)
+                     : "memory");
+    }
+  }
+  // Programmatic dependent launch: wait until the previous kernel on the
+  // stream has completed and its memory is visible. Nothing is loaded or
+  // stored before the wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // The first push's shard loads do not depend on the parity: start them
   // before anything else, so that their latency overlaps the parity and
   // status reads.
   V x0[VPT];
-  UnitPos p0{};
-  const bool push0 = iters > 0 && g < N;
-  if (push0) {
-    p0 = unit_pos<VPT>(a, g, lane);
-    if (p0.r != a.skip_rank) {
-      const V* src = reinterpret_cast<const V*>(a.shard[p0.r]) + p0.src;
+  if (push0 && p0.r != a.skip_rank) {
+    const V* src = reinterpret_cast<const V*>(a.shard[p0.r]) + p0.src;
 #pragma unroll
-      for (int v = 0; v < VPT; ++v)
-        if (p0.idx + 32 * v < a.wv) x0[v] = E::ld_shard(src + 32 * v);
-    }
+    for (int v = 0; v < VPT; ++v)
+      if (p0.idx + 32 * v < a.wv) x0[v] = E::ld_shard(src + 32 * v);
   }
   // Device-resident parity: this warp's own copy (one load per warp of one
   // address, so every lane sees the same value).

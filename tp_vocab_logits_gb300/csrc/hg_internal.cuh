@@ -64,6 +64,9 @@ struct GatherArgs {
   // When the next kernel on the stream may start launching: 0 early (once the
   // first loads are issued), 1 late (once each warp's work is done).
   int late_trigger = 0;
+  // 1: before waiting on the previous kernel, each CTA prefetches its first
+  // push unit of the shards into L2 (shards in device memory only).
+  int l2_prefetch = 0;
 };
 
 // Launch shape of one row count: CTAs (32 * tp threads each), elements per lane

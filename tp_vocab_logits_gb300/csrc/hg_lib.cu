@@ -294,8 +294,11 @@ int hg_destroy(hg_handle* h) {
 
 namespace {
 
+// device_shards: the shards are device memory, whose first units the kernel
+// may prefetch into L2 before it waits on the previous kernel (not for
+// page-locked host memory, which the host may still be writing).
 int gather_impl(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
-                hg_row_stats* stats, hg_stream_t stream) {
+                hg_row_stats* stats, hg_stream_t stream, bool device_shards) {
   if (!h || !shard_ptrs || !out_ptrs) return HG_ERR_ARG;
   if (stats && (h->tp > 16 || !h->partials)) return HG_ERR_ARG;
   if (M < 1 || M > h->cap || !h->served[M]) return HG_ERR_ROWS;
@@ -336,6 +339,7 @@ int gather_impl(hg_handle* h, const void* const* shard_ptrs, void* const* out_pt
   a.M = M;
   a.chunks = stats ? h->chunks_stats[M] : h->chunks[M];
   a.skip_rank = h->skip_rank;
+  a.l2_prefetch = device_shards ? 1 : 0;
   if (stats) {
     a.partials = h->partials;
     a.stats = stats;
@@ -454,7 +458,7 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
         shard[r] = base + (size_t)r * M * h->W * 2;
         out[r] = base + (size_t)h->tp * M * h->W * 2 + (size_t)r * M * V * 2;
       }
-      const int st = gather_impl(h, shard.data(), out.data(), M, nullptr, stream);
+      const int st = gather_impl(h, shard.data(), out.data(), M, nullptr, stream, true);
       if (st != HG_OK) return st;
     }
     return (int)HG_OK;
@@ -548,7 +552,7 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
 
 int hg_gather(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
               hg_stream_t stream) {
-  return gather_impl(h, shard_ptrs, out_ptrs, M, nullptr, stream);
+  return gather_impl(h, shard_ptrs, out_ptrs, M, nullptr, stream, true);
 }
 
 namespace {
@@ -587,13 +591,13 @@ int hg_gather_host(hg_handle* h, const void* const* shard_ptrs, void* const* out
     sh[r] = p;
     if (device_view(out_ptrs[r], h->device, &ou[r]) != HG_OK) return HG_ERR_ARG;
   }
-  return gather_impl(h, sh, ou, M, nullptr, stream);
+  return gather_impl(h, sh, ou, M, nullptr, stream, false);
 }
 
 int hg_gather_stats(hg_handle* h, const void* const* shard_ptrs, void* const* out_ptrs, int M,
                     hg_row_stats* stats, hg_stream_t stream) {
   if (!stats) return HG_ERR_ARG;
-  return gather_impl(h, shard_ptrs, out_ptrs, M, stats, stream);
+  return gather_impl(h, shard_ptrs, out_ptrs, M, stats, stream, true);
 }
 
 int hg_sync(hg_handle* h, hg_stream_t stream) {

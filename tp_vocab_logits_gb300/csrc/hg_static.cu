@@ -110,6 +110,7 @@ extern "C" int hg_gather_static(int tp, int shard_cols, const void* const* shard
   a.wv = wv;
   a.M = M;
   a.skip_rank = -1;
+  a.l2_prefetch = 1;
 
   // Launch shape: the library's fixed rule (elements per lane by tp and M,
   // one CTA per unit up to the co-resident maximum, beyond which the CTAs
