@@ -447,3 +447,44 @@ def test_timeout_recovery():
         np.testing.assert_array_equal(from_dev(outs), want)
     assert_mailboxes_armed(h, hg)
     h.close()
+
+
+@pytest.mark.parametrize("tp,W,n_calls,kw", [
+    (8, 20480, 301, {}),
+    (8, 20480, 101, {"device_parity": True}),
+    (4, 4096, 201, {}),
+])
+def test_chain_reads_the_previous_kernels_output(tp, W, n_calls, kw):
+    """Each call's shards are slices of the previous call's outputs, so the
+    previous gather kernel is still writing them when the next call's launch
+    begins (programmatic dependent launch) and prefetches them into L2. Every
+    value read must still be the previous call's result. Two output sets
+    alternate; call i reads set (i - 1) % 2 and writes set i % 2, and rank r's
+    shard is segment (r + shift) % tp of rank r's row, with shift 1 when
+    reading set 0 and 2 when reading set 1: a read of the set's older contents
+    (two calls back) would show a rotation of 3 segments. The final outputs
+    are compared with the oracle run through the same chain."""
+    h = hg.hg_create(tp, W, 1, **kw)
+    og = oracle.Gather(tp, W, 1)
+    bits = synth.shards(41, tp, 1, W, scale=3.0, sent_frac=0.01).numpy().view(np.uint16)
+    bufs = [empty_outs(tp, 1, tp * W), empty_outs(tp, 1, tp * W)]
+    shifts = (1, 2)
+
+    def seg(row, r, src):
+        k = (r + shifts[src]) % tp
+        return row[:, k * W:(k + 1) * W]
+
+    calls = [hg.GatherCall(h, [seg(bufs[src][r], r, src) for r in range(tp)], bufs[1 - src], 1)
+             for src in (0, 1)]
+    hg.GatherCall(h, to_dev(bits), bufs[0], 1)()
+    for i in range(1, n_calls):
+        calls[(i - 1) % 2]()
+    hg.hg_sync(h)
+
+    want = og.call(bits)
+    for i in range(1, n_calls):
+        src = (i - 1) % 2
+        want = og.call(np.ascontiguousarray(np.stack([seg(want[r], r, src) for r in range(tp)])))
+    np.testing.assert_array_equal(from_dev(bufs[(n_calls - 1) % 2]), want)
+    assert_mailboxes_armed(h, hg)
+    h.close()
