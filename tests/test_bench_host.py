@@ -63,3 +63,14 @@ def test_traffic_lookup_follows_the_kernel_hash():
     else:
         assert got is None  # counters of another kernel source are not reported
     assert bench.traffic_from_profile("no_such_workload") is None
+
+
+def test_graph_split_issues_exactly_the_steps():
+    """The timed step's calls are replays of a graph of up to 200 calls plus
+    one graph of the remainder: together exactly `steps` calls."""
+    for steps in (1, 3, 199, 200, 201, 1000, 1001, 4321):
+        n, reps, rem = bench.graph_split(steps)
+        assert 1 <= n <= 200 and 0 <= rem < n
+        assert n * reps + rem == steps
+    assert bench.graph_split(1000) == (200, 5, 0)
+    assert bench.graph_split(50) == (50, 1, 0)
