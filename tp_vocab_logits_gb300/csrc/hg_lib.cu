@@ -419,7 +419,7 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
   constexpr size_t kPoolBytes = 256ull << 20;
   // Row counts above this keep the fixed rule: tuning pays at decode sizes,
   // and at large row counts the fixed rule is near the memory roofline (TP8,
-  // V=163840: 0.98-1.20 of the measured HBM copy rate from M = 32 on).
+  // V=163840: 0.97-1.21 of the measured HBM copy rate from M = 32 on).
   constexpr int kMaxTunedRows = 16;
   constexpr float kBlockUs = 300.f;
   constexpr int kRounds = 3;
