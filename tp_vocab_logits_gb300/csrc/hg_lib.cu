@@ -66,16 +66,7 @@ void free_handle(hg_handle* h) {
   delete h;
 }
 
-// Launch shape for M rows by a fixed rule. One CTA = one warp per virtual
-// rank; each lane carries default_vpt(tp, M) elements (3 for one or two rows
-// at tp <= 8, 4 otherwise, 2 for CTAs of 1024 threads); one CTA per unit up to
-// the co-resident maximum, beyond which the CTAs loop over the units; no
-// prefetch. Measured at TP8, V=163840 (us/call, C loop): M=1 3.3 with 3
-// elements per lane against 3.6 with 4; M = 4, 8, 64: 7.5, 11.3, 90.3 with 4.
-// The best shape depends on tp, W and M in ways no simple rule captures (M=2:
-// 5 elements per lane, 4.5 us; M=64: 5, 87.4 us), so hg_options.autotune times
-// the candidates. The grid never exceeds the co-resident CTA count, which the
-// kernel's cross-CTA polls need.
+// Range checks of the launch-shape options.
 int check_shape_options(const hg_handle* h, const hg_options* opt) {
   if (!opt) return HG_OK;
   const int v = opt->elems_per_lane;
@@ -95,6 +86,14 @@ int max_grid(const hg_handle* h, const hg::LaunchShape& s, long long* g) {
   return HG_OK;
 }
 
+// Launch shape for M rows by the fixed rule, unless the options force part of
+// it: one CTA = one warp per virtual rank; each lane carries default_vpt(tp, M)
+// elements (3 for one or two rows at tp <= 8, 4 otherwise, 2 for CTAs of 1024
+// threads; the statistics kernel: stats_vpt); one CTA per unit up to the
+// co-resident maximum, beyond which the CTAs loop over the units; no prefetch.
+// The best shape depends on tp, W and M in ways no simple rule captures, so
+// hg_options.autotune can time the candidates instead. The grid never exceeds
+// the co-resident CTA count, which the kernel's cross-CTA polls need.
 int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchShape* out,
              int* chunks_out) {
   const int forced_vpt = opt ? opt->elems_per_lane : 0;
