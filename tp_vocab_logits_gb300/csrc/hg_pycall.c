@@ -122,7 +122,8 @@ static PyObject *call_call(PyObject *obj, PyObject *args, PyObject *kwds) {
     PyErr_SetString(PyExc_TypeError, "a gather call takes no arguments");
     return NULL;
   }
-  /* A closed handle has ptr None: pass NULL, which the library rejects. */
+  /* A closed handle has ptr 0 (None is taken the same way): pass NULL, which
+     the library rejects. */
   PyObject *p = PyObject_GetAttr(self->handle, g_ptr_name);
   if (!p) return NULL;
   void *h = p == Py_None ? NULL : PyLong_AsVoidPtr(p);
