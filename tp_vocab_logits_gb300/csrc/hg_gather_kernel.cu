@@ -394,6 +394,12 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   UnitPos p0{};
   const bool push0 = iters > 0 && g < N;
   if (push0) p0 = unit_pos<VPT>(a, g, lane);
+  // This warp's pointers come from the kernel arguments, which no kernel
+  // writes, so they may be read before the wait.
+  const V* const src0 =
+      reinterpret_cast<const V*>(a.shard[push0 ? p0.r : 0]) + (push0 ? p0.src : 0);
+  V* const box0 = reinterpret_cast<V*>(a.box[d]);
+  V* const out = reinterpret_cast<V*>(a.out[d]);
   // Before the wait, only an L2 prefetch of that unit (16-byte vectors), so
   // that its DRAM round trip overlaps the previous kernel. It brings no value
   // into the SM, and every access to device memory goes through L2, so the
@@ -404,14 +410,20 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
     if (a.l2_prefetch && threadIdx.x == 0 && push0 && p0.r != a.skip_rank) {
       const int n = min(32 * VPT, a.wv - p0.idx);
       if (n > 0)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                     ::"l"(reinterpret_cast<const V*>(a.shard[p0.r]) + p0.src), "r"(n * 16)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src0), "r"(n * 16)
                      : "memory");
     }
   }
+  // With the early trigger this launch usually starts while the previous
+  // kernel still runs: have the pointers in registers before the wait (the
+  // empty asm takes them as operands), off the path that starts when that
+  // kernel completes. With the late trigger it starts as the previous kernel
+  // ends; there the loads keep the compiler's schedule (forcing them, or
+  // moving them after the wait, measured slower at two rows).
+  if (!a.late_trigger) asm volatile("" ::"l"(src0), "l"(box0), "l"(out));
   // Programmatic dependent launch: wait until the previous kernel on the
-  // stream has completed and its memory is visible. Nothing is loaded or
-  // stored before the wait.
+  // stream has completed and its memory is visible. Apart from the L2
+  // prefetch, nothing reads or writes global memory before the wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // The first push's shard loads do not depend on the parity: start them
@@ -419,10 +431,9 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   // status reads.
   V x0[VPT];
   if (push0 && p0.r != a.skip_rank) {
-    const V* src = reinterpret_cast<const V*>(a.shard[p0.r]) + p0.src;
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
-      if (p0.idx + 32 * v < a.wv) x0[v] = E::ld_shard(src + 32 * v);
+      if (p0.idx + 32 * v < a.wv) x0[v] = E::ld_shard(src0 + 32 * v);
   }
   // Device-resident parity: this warp's own copy (one load per warp of one
   // address, so every lane sees the same value).
@@ -436,8 +447,7 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   // One load per warp of one address: every lane sees the same value.
   if (ld_relaxed_s32(a.status) != kDevOk) return;  // unrecovered error: no work
 
-  V* const box = reinterpret_cast<V*>(a.box[d]) + (size_t)parity * a.parity_stride;
-  V* const out = reinterpret_cast<V*>(a.out[d]);
+  V* const box = box0 + (size_t)parity * a.parity_stride;
 
   // Iteration 0's push, from the loads started above.
   if (push0 && p0.r != a.skip_rank) {
