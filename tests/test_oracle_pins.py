@@ -310,6 +310,8 @@ MUTANTS = {
     "slice_wrong_stride": ("out[(size_t)m * V + c]", "out[(size_t)m * v_real + c]"),
     "stats_last_argmax": ("if (x > mx) { mx = x; arg = c; }", "if (x >= mx) { mx = x; arg = c; }"),
     "stats_sum_without_shift": ("s += std::exp(x - mx);", "s += std::exp(x);"),
+    "stats_sum_unguarded": ("if (x != -std::numeric_limits<double>::infinity()) s += std::exp(x - mx);",
+                            "s += std::exp(x - mx);"),
 }
 
 
