@@ -1,6 +1,7 @@
 """Host-side logic of bench.py, without a GPU: the algorithmic-byte formula,
-the number of rotating input sets, the output check, the replica arithmetic
-and the lookup of the profiled DRAM traffic."""
+the number of rotating input sets, the output check, the replica arithmetic,
+the lookup of the profiled DRAM traffic, the graph split of the timed calls,
+and the reference arm's JSON line (the CPU oracle runs without a GPU)."""
 
 import hashlib
 import json
@@ -12,6 +13,7 @@ import torch
 import bench
 
 S = -(1 << 31)  # the sentinel word as a signed int32
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_algorithmic_bytes_formula():
@@ -74,3 +76,47 @@ def test_graph_split_issues_exactly_the_steps():
         assert n * reps + rem == steps
     assert bench.graph_split(1000) == (200, 5, 0)
     assert bench.graph_split(50) == (50, 1, 0)
+
+
+def _run_bench(args, env_extra=None):
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, env=env,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm (the CPU oracle on the step workload) prints one JSON
+    line with the contract's keys, on the same config, metric and unit."""
+    r = _run_bench(["--impl", "reference", "--steps", "3", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "us/call"
+    assert d["higher_is_better"] is False and d["scaling"] == "weak"
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["config"] == bench.workload_config()
+    assert d["value"] > 0 and abs(d["ms_per_step"] * 1000 - d["value"]) < 1e-2
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "us/call", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    """Under torchrun only rank 0 runs and prints the reference arm."""
+    r = _run_bench(["--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
+
+
+def test_bench_rejects_too_few_warmup_steps():
+    r = _run_bench(["--impl", "reference", "--steps", "3", "--warmup", "2"])
+    assert r.returncode != 0 and "warmup" in r.stderr
