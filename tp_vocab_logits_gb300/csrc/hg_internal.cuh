@@ -80,6 +80,13 @@ struct LaunchShape {
   bool late = false;   // trigger the next launch late (see trigger_late)
 };
 
+// The kernel indexes units with int: a CTA's push index t * G + g runs up to
+// N + 3G (the shard loads of iteration t + 1 included), so a launch of N units
+// on at most max_ctas CTAs must keep N + 3 * max_ctas within int.
+inline bool units_fit_int(long long units, long long max_ctas) {
+  return units + 3 * max_ctas <= 0x7fffffffLL;
+}
+
 // When to let the next kernel on the stream start launching, for a grid of
 // `ctas` CTAs that loops over `units` units with at most `max_ctas`
 // co-resident: early (the next grid fits beside this one, or this launch runs

@@ -113,6 +113,7 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchS
   long long maxg = 0;
   const int st = max_grid(h, s, &maxg);
   if (st != HG_OK) return st;
+  if (!hg::units_fit_int(units, maxg)) return HG_ERR_ARG;
   long long G = want < maxg ? want : maxg;
   if (G < 1) G = 1;
   s.ctas = (int)G;
@@ -381,6 +382,7 @@ int tune_candidates(hg_handle* h, int M, const hg_options* opt, std::vector<Cand
       long long maxg = 0;
       const int st = max_grid(h, c.s, &maxg);
       if (st != HG_OK) return st;
+      if (!hg::units_fit_int(units, maxg)) continue;
       std::vector<long long> grids;
       if (opt->ctas) {
         long long g = opt->ctas < units ? opt->ctas : units;
