@@ -152,7 +152,8 @@ static PyTypeObject CallType = {
 };
 
 static struct PyModuleDef hgcall_module = {
-    PyModuleDef_HEAD_INIT, "_hgcall", "Direct hg_gather calls for the Python binding.", -1, NULL,
+    PyModuleDef_HEAD_INIT, "_hgcall", "Direct hg_gather calls for the Python binding.", -1,
+    NULL /* methods */, NULL /* slots */, NULL /* traverse */, NULL /* clear */, NULL /* free */,
 };
 
 PyMODINIT_FUNC PyInit__hgcall(void) {
