@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from tp_vocab_logits_gb300 import _build, hg
 
@@ -88,3 +89,18 @@ def test_direct_call_object_marshals_and_raises(lib):
         call(1)
     with pytest.raises(ValueError):
         mod.Call(fn, Closed(), [16, 32], [48], 1, 0, None, on_error)
+
+
+def test_binding_rejects_bad_tensor_lists_before_the_library():
+    """GatherCall checks the tensor lists before anything reaches libhg: a
+    list of the wrong length, and host tensors that are not page-locked (the
+    kernel can only read and write host memory that is). The dtype and shape
+    checks after these need page-locked or device tensors; the GPU tests
+    cover them (test_rejected_calls_change_nothing)."""
+    h = hg.Handle(0, 2, 8, 1, None)  # never handed to the library here
+    shards = [torch.zeros(1, 8, dtype=torch.int16) for _ in range(2)]
+    outs = [torch.zeros(1, 16, dtype=torch.int16) for _ in range(2)]
+    with pytest.raises(ValueError, match="expected 2 tensors"):
+        hg.GatherCall(h, shards[:1], outs, 1)
+    with pytest.raises(ValueError, match="page-locked"):
+        hg.GatherCall(h, shards, outs, 1)
