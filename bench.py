@@ -669,7 +669,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic",
-        "config": workload_config({
+        "config": workload_config(),
+        "measurement": {
             "l2": f"inputs+outputs rotate over {nsets} sets "
                   f"({nsets * TP * M_STEP * W * 2 * (1 + TP) / 2**20:.0f} MiB > 129 MB L2); "
                   "mailboxes (42 MB) are the method's persistent state",
@@ -677,7 +678,7 @@ def run_ours(args):
                            shapes="autotuned at hg_create" if tune else "fixed rule"),
             "issue": "the timed calls replay CUDA graphs of up to 200 captured calls on a "
                      "handle with device-resident parity, as a captured decode step issues "
-                     "them; eager_us_per_call: the same calls issued one by one from Python"}),
+                     "them; eager_us_per_call: the same calls issued one by one from Python"},
         "gpu_launches": args.steps,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
                 "h2d_bytes_per_step": TP * M_STEP * W * 2,

@@ -131,7 +131,9 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int *rows, int nrows,
                  const hg_options *opt, hg_handle **out);
 
 /* Free the mailboxes and the handle; waits for the device first. NULL is a
- * no-op. Always returns HG_OK unless freeing fails (HG_ERR_CUDA). */
+ * no-op. Always returns HG_OK unless freeing fails (HG_ERR_CUDA).
+ * The pages have no counterpart: HeadGather's mailbox lives as long as the
+ * model that installed it. */
 int hg_destroy(hg_handle *h);
 
 /*
@@ -203,13 +205,16 @@ int hg_gather_host(hg_handle *h, const void *const *shard_ptrs, void *const *out
 
 /* Wait for `stream`, then read the device status word. Returns HG_OK,
  * HG_ERR_TIMEOUT (a poll gave up; mailbox contents undefined until hg_rearm)
- * or HG_ERR_CUDA. */
+ * or HG_ERR_CUDA. Failure detection of this library; the pages have no
+ * counterpart (their polls are unbounded). */
 int hg_sync(hg_handle *h, hg_stream_t stream);
 
 /* Recovery after an error: refill every mailbox word of both parities with
  * the sentinel, re-arm the statistics cells and the fused producer's split
  * cells, clear the status words and set the parity to 0 (host and device
- * copies), on `stream`, asynchronously. */
+ * copies), on `stream`, asynchronously. It restores the state that
+ * HeadGather.__init__ leaves (mailboxes armed with PAIR_SENT, parity 0);
+ * recovery itself has no counterpart on the pages. */
 int hg_rearm(hg_handle *h, hg_stream_t stream);
 
 /* Parity the next hg_gather uses (0 or 1; starts at 0, flips per served call
@@ -219,13 +224,16 @@ int hg_parity(const hg_handle *h);
 
 /* Rank `rank`'s mailbox for inspection: device pointer to [2][cap][tp * W]
  * BF16 (parity-major) and its size in bytes. Owned by the handle; read it only
- * while no gather is in flight. Errors: HG_ERR_ARG. */
+ * while no gather is in flight. Errors: HG_ERR_ARG. Test surface: the layout
+ * is that of LamportRows(group, device, (2, cap, words * tp), PAIR_SENT) in
+ * HeadGather.__init__, but the pages expose no accessor. */
 int hg_mailbox(const hg_handle *h, int rank, const void **dev_ptr, size_t *bytes);
 
 /* Launch shape that hg_gather uses for row count M: CTAs, threads per CTA,
  * elements per lane and whether the next push's shard loads are issued one
  * iteration ahead (1) or not (0). Any output pointer may be NULL. Errors:
- * HG_ERR_ARG, HG_ERR_ROWS. */
+ * HG_ERR_ARG, HG_ERR_ROWS. Inspection only; the pages' counterpart,
+ * gather_ctas(m, ...) in HeadGather.__init__, is named but not printed. */
 int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *elems_per_lane,
                     int *prefetch);
 
@@ -236,7 +244,7 @@ int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *ele
  * it off). The pollers of the other ranks
  * then wait for words that never arrive and give up after the poll bound;
  * hg_sync reports HG_ERR_TIMEOUT. No device fault, trap or endless wait is
- * involved. Errors: HG_ERR_ARG.
+ * involved. Errors: HG_ERR_ARG. No counterpart on the pages.
  */
 int hg_debug_skip_push(hg_handle *h, int rank);
 
@@ -288,7 +296,8 @@ int hg_stock_gather(int tp, int shard_cols, const void *const *shard_ptrs,
                     void *const *out_ptrs, int M, hg_stream_t stream);
 
 /* Largest mailbox that one hg_gather_static call may use, in bytes:
- * tp * M * tp * shard_cols * 2 (every rank's [M, V] BF16 rows, one parity). */
+ * tp * M * tp * shard_cols * 2 (every rank's [M, V] BF16 rows, one parity).
+ * At TP8, V=163840 (shard_cols 20480) that is up to M = 9 rows. */
 #define HG_STATIC_MAILBOX_BYTES (24u * 1024u * 1024u)
 
 /*
@@ -316,15 +325,18 @@ int hg_stock_gather(int tp, int shard_cols, const void *const *shard_ptrs,
  *                   reported
  *   stream          the stream of the call
  *
- * Same result as hg_gather on the same shards. The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress, with that device
- * current), so make that first call before any stream capture. Every call
+ * Same result as hg_gather on the same shards. The call works on the device
+ * that is current when it is made: `stream` and every pointer must belong to
+ * that device (a stream of another device gives HG_ERR_ARG). The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current), so make that first call before any stream capture. Every call
  * shares the array and finds it as the previous call left it: each call clears
  * the status words and re-arms its mailbox region before gathering, on
  * `stream`. Calls whose device work overlaps (other streams or threads) race on
  * the array. No parity state is kept. Errors, before any device work:
- * HG_ERR_ARG (bad sizes, NULL or misaligned pointers, or a mailbox larger than
- * HG_STATIC_MAILBOX_BYTES), HG_ERR_CUDA (device lookup or launch failed).
+ * HG_ERR_ARG (bad sizes, NULL or misaligned pointers, a mailbox larger than
+ * HG_STATIC_MAILBOX_BYTES, or a stream of another device), HG_ERR_CUDA
+ * (device lookup or launch failed).
  */
 int hg_gather_static(int tp, int shard_cols, const void *const *shard_ptrs,
                      void *const *out_ptrs, int M, int *status_out, hg_stream_t stream);
@@ -354,7 +366,8 @@ typedef struct hg_row_stats {
 int hg_gather_stats(hg_handle *h, const void *const *shard_ptrs, void *const *out_ptrs, int M,
                     hg_row_stats *stats, hg_stream_t stream);
 
-/* Human-readable text of a status code; never NULL. */
+/* Human-readable text of a status code; never NULL. No counterpart on the
+ * pages (HeadGather reports failures as Python exceptions). */
 const char *hg_strerror(int status);
 
 #ifdef __cplusplus

@@ -33,7 +33,7 @@ def test_bench_line_carries_the_contract_keys():
     assert d["n_gpus"] == 1 and d["steps"] == steps and d["warmup"] == 3
     assert d["gpu_launches"] == steps
     assert d["value"] > 0 and abs(d["ms_per_step"] * 1000 - d["value"]) < 1e-2
-    assert "workload" in d["config"] and "issue" in d["config"]
+    assert "workload" in d["config"] and "issue" in d["measurement"]
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 8 * 20480 * 2          # every rank's [1, W] shard

@@ -5,6 +5,9 @@ path and the 4-byte word path occur, with ragged units), a cap, a sequence of
 row counts, and a launch shape (elements per lane 1..6, a grid that may be
 tiny, prefetch on or off, or the autotuner). Every call is compared with the
 oracle word for word; mailboxes and parity are checked after the sequence.
+Besides the sentinel and the zero pairs, the inputs carry the generator's
+other classes next to the sentinel (swapped zero halves, one-bit neighbours,
+NaN and infinity pairs) at 2 %.
 """
 
 import random
@@ -53,7 +56,8 @@ def test_random_configuration_vs_oracle(case):
     og = oracle.Gather(tp, W, cap)
     for i, M in enumerate(c["Ms"]):
         bits = synth.shards(50 + case, tp, M, W, scale=3.0, sent_frac=0.03, zero_frac=0.01,
-                            negzero_frac=0.01, set_index=i).numpy().view(np.uint16)
+                            negzero_frac=0.01, extra_frac=0.02,
+                            set_index=i).numpy().view(np.uint16)
         want = og.call(bits)
         outs = empty_outs(tp, M, tp * W)
         hg.hg_gather(h, to_dev(bits), outs, M)

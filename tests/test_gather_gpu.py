@@ -18,7 +18,7 @@ import torch
 import oracle
 from tp_vocab_logits_gb300 import hg, synth
 
-from helpers import S_I32, assert_mailboxes_armed, empty_outs, from_dev, rewrite_concat, to_dev
+from helpers import assert_mailboxes_armed, empty_outs, from_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -201,13 +201,15 @@ def test_wide_tp_vs_oracle(tp):
 
 def test_config2_decode_m1():
     """TP8, V=163840, cap=8, M=1: 1000 calls back to back on one stream with
-    0.1 % sentinel words, rotating three input sets; every call's outputs
-    against the oracle word for word (each call gathers into its own slot of
-    a ring of outputs, checked once the ring is full), mailboxes at the end."""
+    0.1 % sentinel words (and, beyond the workload's recipe, 0.1 % of the
+    generator's other classes next to the sentinel), rotating three input
+    sets; every call's outputs against the oracle word for word (each call
+    gathers into its own slot of a ring of outputs, checked once the ring is
+    full), mailboxes at the end."""
     tp, W, cap, calls, ring = 8, 20480, 8, 1000, 50
     h = hg.hg_create(tp, W, cap)
     og = oracle.Gather(tp, W, cap)
-    sets = [synth.shards(1, tp, 1, W, scale=3.0, sent_frac=0.001, set_index=i)
+    sets = [synth.shards(1, tp, 1, W, scale=3.0, sent_frac=0.001, extra_frac=0.001, set_index=i)
             .numpy().view(np.uint16) for i in range(3)]
     dev = [to_dev(s) for s in sets]
     outs = [empty_outs(tp, 1, tp * W) for _ in range(ring)]
@@ -266,24 +268,46 @@ def test_config4_small_points_vs_oracle(tp, W, M):
                  negzero=0.0, seed=3)
 
 
+def _host_bytes_available() -> int:
+    with open("/proc/meminfo") as f:
+        for line in f:
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    return 0
+
+
 @pytest.mark.parametrize("tp,W,M", [(8, 20480, 64), (8, 20480, 256), (16, 65536, 64),
                                     (16, 4096, 256), (4, 65536, 128)])
-def test_config4_large_points_properties(tp, W, M):
-    """Full-size sweep points: every output equals the rank-order concat with
-    sentinel words sent as zero (the definition's property at any size), and
-    every mailbox is re-armed, over three calls (both parities)."""
+def test_config4_large_points_vs_oracle(tp, W, M):
+    """Full-size sweep points (cap = M, U(-20, 20), with 0.1 % sentinel words
+    and 0.1 % of the other classes next to it): every output word of every
+    rank against the oracle run through the same three calls (both parities),
+    and every mailbox re-armed, as the oracle's are. The oracle holds every
+    rank's two-parity mailbox in host memory (up to 4.3 GB, at TP16 with
+    65536-column shards and M=64); a point whose oracle state would not fit in
+    the host's available memory is skipped, and says so."""
+    V = tp * W
+    need = tp * 2 * M * V * 2 + 2 * tp * M * V * 2 + tp * M * W * 2
+    avail = _host_bytes_available()
+    if 1.5 * need > avail:
+        pytest.skip(f"the oracle needs {need / 2**30:.1f} GiB of host memory, "
+                    f"{avail / 2**30:.1f} GiB available")
     h = hg.hg_create(tp, W, M)
-    outs = empty_outs(tp, M, tp * W)
+    og = oracle.Gather(tp, W, M)
+    outs = empty_outs(tp, M, V)
     for i in range(3):
         bits = synth.shards(3, tp, M, W, dist="uniform", scale=20.0, sent_frac=0.001,
-                            set_index=i, device="cuda")
-        shards = [bits[r] for r in range(tp)]
-        hg.hg_gather(h, shards, outs, M)
+                            extra_frac=0.001, set_index=i, device="cuda")
+        want = og.call(bits.cpu().numpy().view(np.uint16))
+        hg.hg_gather(h, [bits[r] for r in range(tp)], outs, M)
         hg.hg_sync(h)
-        want = rewrite_concat(shards)
+        assert hg.hg_parity(h) == og.parity
         for d in range(tp):
-            assert torch.equal(outs[d].view(torch.int32), want), f"call {i} rank {d}"
-        assert not any((o.view(torch.int32) == S_I32).any().item() for o in outs)
+            got = outs[d].cpu().numpy().view(np.uint16)
+            if not np.array_equal(got, want[d]):
+                raise AssertionError(f"call {i} rank {d}: "
+                                     f"{int((got != want[d]).sum())} bf16 columns differ")
+        del want
     assert_mailboxes_armed(h, hg)
     h.close()
 

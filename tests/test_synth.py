@@ -67,3 +67,25 @@ def test_normal_values_have_the_requested_spread():
     u = synth.shards(5, 8, 4, 4096, dist="uniform", scale=20.0).view(torch.bfloat16).float()
     assert u.min().item() >= -20.0 and u.max().item() <= 20.0
     assert abs(u.std().item() - 20.0 / 3 ** 0.5) < 0.2
+
+
+def test_extra_word_classes():
+    """extra_frac injects each word of EXTRA_WORDS at an equal share, leaves
+    the other words as they were, and with 0 changes nothing."""
+    kw = dict(scale=2.0, sent_frac=0.02, zero_frac=0.01, negzero_frac=0.01, set_index=2)
+    base = synth.shards(13, 2, 8, 4096, **kw)
+    assert torch.equal(synth.shards(13, 2, 8, 4096, extra_frac=0.0, **kw), base)
+    ex = synth.shards(13, 2, 8, 4096, extra_frac=0.14, **kw)
+    b = base.numpy().view(np.uint32)
+    e = ex.numpy().view(np.uint32)
+    changed = b != e
+    n = e.size
+    assert abs(np.count_nonzero(changed) / n - 0.14) < 0.01
+    for word in synth.EXTRA_WORDS:
+        assert word != 0x80000000
+        frac = np.count_nonzero(e[changed] == word) / n
+        assert abs(frac - 0.02) < 0.004, (hex(word), frac)
+    assert set(np.unique(e[changed]).tolist()) <= set(synth.EXTRA_WORDS)
+    # slices regenerate alone with the extra classes too
+    part = synth.shards(13, 1, 3, 16, extra_frac=0.14, rank0=1, row0=2, col0=32, **kw)
+    assert torch.equal(part, ex[1:2, 2:5, 32:48])

@@ -47,8 +47,11 @@
 // overlaps the weight stream; the last one or two tiles are consumed by all
 // threads after the CTA's own tiles. Every wait in this kernel (mbarriers and
 // polls) is bounded by %globaltimer; on expiry the kernel records the error
-// in the status block, lets its in-flight copies and MMAs drain, frees its
-// tensor memory and returns.
+// in the status block and stops issuing work. Before it frees its tensor
+// memory and returns, the TMA thread waits for every copy it issued to land
+// (the full barrier of each stage it filled) and the MMA thread for every MMA
+// it issued to complete (a final commit): those waits end because that work
+// needs nothing from any other CTA, so they are bounded by time only.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -260,6 +263,21 @@ __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FusedArgs& a, in
   }
 }
 
+// Wait for work this CTA issued itself (TMA copies into its shared memory,
+// its MMAs). That work completes without any other CTA, so the wait does not
+// give up when another CTA raises an error; it is bounded by time alone, and
+// on expiry it records the error and returns false (a last resort).
+__device__ bool mbar_wait_own(uint64_t* bar, uint32_t parity, const FusedArgs& a, int where) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      raise_error(a, where);
+      return false;
+    }
+  }
+  return true;
+}
+
 // One work item of a CTA: a tile (rank r's vocab rows t * 128 ..) and the
 // K-block range [kb0, kb1) it covers; part -1 for a whole tile, else the
 // part of split tail tile j.
@@ -410,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       const uint64_t pol_h = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
+      int issued = 0;  // stage fills issued; fill j goes to stage j % kStages
       bool ok = true;
       for (int i = 0; i < n_items && ok; ++i) {
         const Item w = item_at(a, g, G, i, kblocks);
@@ -422,8 +441,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
                       &sh->full[stage], pol_w);
           tma_load_2d(sB + (size_t)stage * kBBytes, &a.tm_h[r], kb * kBlockK, 0,
                       &sh->full[stage], pol_h);
+          ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+      }
+      // Every copy issued must land before the CTA's shared memory goes: wait
+      // for the last fill of each stage (fill j completes the phase of parity
+      // (j / kStages) & 1 of stage j % kStages; a stage is refilled only after
+      // its previous fill was consumed, so no later phase can be pending).
+      // After a normal run the MMA thread has already seen every fill land.
+      const int last = issued - 1;
+      for (int s = 0; s < kStages && s <= last; ++s) {
+        const int j = last - (last - s) % kStages;
+        mbar_wait_own(&sh->full[s], (uint32_t)((j / kStages) & 1), a, 8);
       }
     }
   } else if (warp == 1) {
@@ -457,9 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
         mma_commit(&sh->acc_full[acc]);  // accumulator ready
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
-      // Let every MMA this thread issued finish before TMEM is freed.
+      // Every MMA this thread issued must complete before TMEM is freed (and
+      // before the stages they read go): a commit tracks all of them.
       mma_commit(&sh->drain);
-      mbar_wait(&sh->drain, 0, a, 4);
+      mbar_wait_own(&sh->drain, 0, a, 4);
     }
   } else {
     // Epilogue: warps 2..5; warp w reads TMEM lanes 32 * (w % 4) ...
@@ -580,12 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
                    "r"(parity ^ 1)
                    : "memory");
   }
-  if (failed) {
-    // Let in-flight TMA copies and MMAs land before the CTA's memory goes.
-    const unsigned long long t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 200000ull) {
-    }
-  }
+  // The TMA thread and the MMA thread waited for their own copies and MMAs
+  // above, before the barrier: nothing is in flight into shared or tensor
+  // memory here.
   if (warp == 1) {
     __syncwarp();  // the warp-wide dealloc needs the whole warp converged
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -649,13 +677,12 @@ size_t split_cells_needed(int sms) {
 
 cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   FusedArgs a;  // copied into the launch by cudaLaunchKernelExC
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // The dynamic shared-memory limit is a per-device attribute of the kernel:
+  // set it on every launch, on the current device (a host call of well under
+  // a microsecond beside a launch that streams the weights for hundreds).
+  cudaError_t e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
   for (int r = 0; r < l.tp; ++r) {
     if (!encode(&a.tm_w[r], l.weight[r], (uint64_t)l.W, (uint64_t)l.K, kTileN) ||
         !encode(&a.tm_h[r], l.hidden[r], (uint64_t)l.M, (uint64_t)l.K, kMmaN))
@@ -682,8 +709,7 @@ cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   a.tiles_per_rank = l.W / kTileN;
   const int items = l.tp * a.tiles_per_rank;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel, kThreads,
-                                                                kSmemBytes);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel, kThreads, kSmemBytes);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int grid = sms * per_sm;

@@ -15,7 +15,9 @@
 // is only a stand-in. Its device address comes from cudaGetSymbolAddress, taken
 // once per device, with that device current, by the first call made on that
 // device (so the first call on a device should be made before any stream
-// capture). The caller passes the shards and outputs as for hg_gather.
+// capture). The caller passes the shards and outputs as for hg_gather; they and
+// the stream belong to the device that is current at the call (a stream of
+// another device is refused).
 //
 // Every call shares the array and finds it as the last call left it. Each call
 // therefore clears the status words and re-arms the mailbox region it uses
@@ -95,6 +97,18 @@ extern "C" int hg_gather_static(int tp, int shard_cols, const void* const* shard
   DeviceScratch ds;
   int st = scratch_for_current_device(&ds);
   if (st != HG_OK) return st;
+  // The array's address and the launches belong to the current device, so the
+  // stream must too. The legacy and per-thread default streams always do.
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cs != nullptr && cs != cudaStreamLegacy && cs != cudaStreamPerThread) {
+    int dev = -1, sdev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HG_ERR_CUDA;
+    if (cudaStreamGetDevice(cs, &sdev) != cudaSuccess) {
+      cudaGetLastError();  // an unknown stream handle: clear the error it set
+      return HG_ERR_ARG;
+    }
+    if (sdev != dev) return HG_ERR_ARG;
+  }
 
   const int wv = vec16 ? shard_cols / 8 : shard_cols / 2;
   const size_t rank_bytes = (size_t)M * tp * shard_cols * 2;  // one rank's [M][V]

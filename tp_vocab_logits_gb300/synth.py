@@ -35,8 +35,16 @@ PAIR_POS_POS_ZERO = 0x00000000
 PAIR_NEG_NEG_ZERO = 0x80008000
 BF16_NEG_INF = 0xFF80
 
+# Further 32-bit words next to the sentinel, injected on request (extra_frac):
+# the pair (-0, +0) (the sentinel's halves swapped), words one bit away from
+# the sentinel (lowest bit; lowest bit of the high half; the bit below the
+# sign), a NaN pair, and the pairs (-inf, -inf) and (+inf, +inf). None of
+# them is the sentinel, so each must move unchanged.
+EXTRA_WORDS = (0x00008000, 0x80000001, 0x80010000, 0xC0000000, 0x7FC07FC0, 0xFF80FF80,
+               0x7F807F80)
+
 # Stream ids (one per use of randomness).
-_S_U1, _S_U2, _S_INJECT = 1, 2, 3
+_S_U1, _S_U2, _S_INJECT, _S_EXTRA, _S_EXTRA_PICK = 1, 2, 3, 4, 5
 # Tensor kinds, folded into the key so that kinds never share a stream.
 KIND_SHARD, KIND_HIDDEN, KIND_WEIGHT, KIND_SEQUENCE = 1, 2, 3, 4
 
@@ -95,14 +103,17 @@ def _grid(shape, shifts, offsets, device) -> torch.Tensor:
 
 def shards(seed: int, tp: int, M: int, W: int, *, dist: str = "normal", scale: float = 1.0,
            sent_frac: float = 0.0, zero_frac: float = 0.0, negzero_frac: float = 0.0,
-           set_index: int = 0, rank0: int = 0, row0: int = 0, col0: int = 0,
-           v_real: int | None = None, device="cpu") -> torch.Tensor:
+           extra_frac: float = 0.0, set_index: int = 0, rank0: int = 0, row0: int = 0,
+           col0: int = 0, v_real: int | None = None, device="cpu") -> torch.Tensor:
     """Logits shards of tp virtual ranks as bf16 bits: int16 [tp, M, W].
 
     dist "normal": bf16(N(0, scale^2)); dist "uniform": bf16(U(-scale, scale)).
     Then each 32-bit word (bf16 columns 2k, 2k+1) independently becomes, with
     probability sent_frac, the pair (+0, -0); with probability zero_frac the
-    pair (+0, +0); with probability negzero_frac the pair (-0, -0).
+    pair (+0, +0); with probability negzero_frac the pair (-0, -0). After
+    that, each word independently becomes, with probability extra_frac, one of
+    EXTRA_WORDS, each of them equally likely (separate random streams: with
+    extra_frac 0 the result is the same as without it).
     v_real: real vocab width of a padded vocab; columns at or beyond it of the
     full [M, tp*W] row hold bf16 -inf.
     rank0/row0/col0 offset the indices, so a slice of a larger tensor can be
@@ -133,6 +144,16 @@ def shards(seed: int, tp: int, M: int, W: int, *, dist: str = "normal", scale: f
         words = torch.where(u < t1, as_i32(PAIR_POS_NEG_ZERO), words)
         words = torch.where((u >= t1) & (u < t2), as_i32(PAIR_POS_POS_ZERO), words)
         words = torch.where((u >= t2) & (u < t3), as_i32(PAIR_NEG_NEG_ZERO), words)
+        bits = words.view(torch.int16).view(tp, M, W)
+    if extra_frac:
+        words = bits.view(torch.int32)
+        wcnt = _grid((tp, M, W // 2), (44, 32, 0), (rank0, row0, col0 // 2), device) + base
+        u = _uniform(wcnt, seed, KIND_SHARD, _S_EXTRA)
+        pick = (_uniform(wcnt, seed, KIND_SHARD, _S_EXTRA_PICK) * len(EXTRA_WORDS)).to(torch.int64)
+        pick = torch.clamp(pick, max=len(EXTRA_WORDS) - 1)
+        table = torch.tensor([v - (1 << 32) if v >= (1 << 31) else v for v in EXTRA_WORDS],
+                             dtype=torch.int32, device=device)
+        words = torch.where(u < extra_frac, table[pick], words)
         bits = words.view(torch.int16).view(tp, M, W)
     if v_real is not None:
         col = (torch.arange(tp, device=device).view(tp, 1, 1) + rank0) * W \
