@@ -365,6 +365,48 @@ def graph_replay_us(torch, hg, synth, tp, W, cap, M, device, stream, calls, rows
     return (us, shape) if with_shape else us
 
 
+def graph_us_per_launch(torch, issue, stream, n_graph=200, reps=5, label="timed_graph"):
+    """us per launch of `issue()` (which enqueues one launch on the current
+    stream), captured n_graph times into one CUDA graph and replayed reps
+    times back to back after 3 untimed replays."""
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for _ in range(n_graph):
+            issue()
+    torch.cuda.synchronize()
+    ms = time_calls(torch, [graph.replay], reps, 3, stream, label)
+    del graph
+    return round(ms * 1000.0 / (reps * n_graph), 3)
+
+
+def latency_floors(torch, hg, shapes, stream, device) -> dict:
+    """The two floor kernels of hg_probe at each launch shape {key: (ctas,
+    threads)}: an empty dependent launch, and the one-vector push -> poll ->
+    copy -> re-arm handoff; us per launch, replayed from CUDA graphs."""
+    res = {}
+    for key, (ctas, threads) in shapes.items():
+        scratch = torch.zeros(hg.hg_probe_scratch_bytes(ctas, threads) // 4 + 4,
+                              dtype=torch.int32, device=device)
+        hg.hg_probe(2, ctas, threads, scratch)
+        hg.hg_probe(1, ctas, threads, scratch)
+        hg.hg_probe(0, ctas, threads)
+        torch.cuda.synchronize()
+        empty = graph_us_per_launch(torch, lambda: hg.hg_probe(0, ctas, threads), stream,
+                                    label="timed_floor_empty")
+        hand = graph_us_per_launch(torch, lambda: hg.hg_probe(1, ctas, threads, scratch),
+                                   stream, label="timed_floor_handoff")
+        torch.cuda.synchronize()
+        n = ctas * threads
+        if int(scratch[8 * n].item()) != 0:
+            raise SystemExit(f"bench: handoff floor kernel timed out ({key})")
+        res[key] = {"ctas": ctas, "threads": threads, "empty_launch_us": empty,
+                    "handoff_us": hand}
+        del scratch
+    return res
+
+
 def graph_split(steps: int, per_graph: int = 200) -> tuple:
     """How `steps` calls are issued as CUDA graphs: (calls per full graph,
     replays of it, calls in one trailing graph (0: none))."""
@@ -402,6 +444,126 @@ class GraphSteps:
     def replays(self) -> list:
         """One replay per list entry; together they issue exactly `steps` calls."""
         return [self.full.replay] * self.reps + ([self.tail.replay] if self.tail else [])
+
+
+def stats_graph_us(torch, hg, synth, M, device, stream, calls=1000) -> dict:
+    """hg_gather_stats at TP8, V=163840, M rows, replayed from CUDA graphs of
+    200 captured calls (device parity), beside the plain gather timed the same
+    way on the same buffers: us per call of each."""
+    import ctypes
+    n = sets_for(TP, W, M)
+    h, sh, ou, cg = make_workload(torch, hg, synth, TP, W, CAP, M, n, device, rows=[M],
+                                  seed=2, device_parity=True)
+    st = hg.new_row_stats(M)
+    lib = hg.load()
+    arrs = [((ctypes.c_void_p * TP)(*[sh[s_, r].data_ptr() for r in range(TP)]),
+             (ctypes.c_void_p * TP)(*[ou[s_, d].data_ptr() for d in range(TP)]))
+            for s_ in range(n)]
+    k = [0]
+
+    def issue_stats():
+        a_ = arrs[k[0] % n]
+        k[0] += 1
+        rc = lib.hg_gather_stats(h.ptr, a_[0], a_[1], M, st.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+        if rc != 0:
+            raise SystemExit(f"hg_gather_stats failed: {hg.strerror(rc)}")
+
+    def issue_plain():
+        a_ = arrs[k[0] % n]
+        k[0] += 1
+        rc = lib.hg_gather(h.ptr, a_[0], a_[1], M, torch.cuda.current_stream().cuda_stream)
+        if rc != 0:
+            raise SystemExit(f"hg_gather failed: {hg.strerror(rc)}")
+    issue_stats()
+    hg.hg_sync(h)
+    reps = max(1, calls // 200)
+    us_s = graph_us_per_launch(torch, issue_stats, stream, reps=reps, label="timed_stats_graph")
+    us_p = graph_us_per_launch(torch, issue_plain, stream, reps=reps, label="timed_plain_graph")
+    hg.hg_sync(h)
+    check_concat(torch, sh[0], ou[0], TP, f"stats graph M={M}")
+    h.close()
+    return {"stats_us": us_s, "plain_us": us_p, "stats_minus_plain_us": round(us_s - us_p, 3)}
+
+
+# The drafter's gather beside the target's (one stream, one decode step = the
+# drafter's gather of its draft block, then the target's gather of the token
+# before it plus the drafted ones): the pages give the drafter no shape; this
+# reads it as the target's tokenizer and TP group with a block of 4 drafted
+# positions.
+DRAFT_M, TARGET_M = 4, 5
+
+
+def drafter_pair(torch, hg, synth, device, stream, warmup, steps=1000) -> dict:
+    """us per decode step of the drafter's gather (TP8, V=163840, M=4) and the
+    target's (M=5) issued back to back on one stream, replayed from CUDA
+    graphs of 100 steps and issued one by one from Python, beside each
+    handle's calls alone (graph-replayed)."""
+    nd = sets_for(TP, W, DRAFT_M)
+    nt = sets_for(TP, W, TARGET_M)
+    hd, sd, od, cd = make_workload(torch, hg, synth, TP, W, 4, DRAFT_M, nd, device,
+                                   rows=[1, 2, 3, 4], seed=31, device_parity=True)
+    ht, st_, ot, ct = make_workload(torch, hg, synth, TP, W, 8, TARGET_M, nt, device,
+                                    rows=[1, 2, 3, 4, 5, 8], seed=32, device_parity=True)
+    cd[0]()
+    ct[0]()
+    hg.hg_sync(hd)
+    hg.hg_sync(ht)
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        pair_calls = []
+        for i in range(100):
+            pair_calls.append(hg.GatherCall(hd, [sd[i % nd, r] for r in range(TP)],
+                                            [od[i % nd, d] for d in range(TP)], DRAFT_M, stream=gs))
+            pair_calls.append(hg.GatherCall(ht, [st_[i % nt, r] for r in range(TP)],
+                                            [ot[i % nt, d] for d in range(TP)], TARGET_M,
+                                            stream=gs))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for c in pair_calls:
+            c()
+    torch.cuda.synchronize()
+    reps = steps // 100
+    ms = time_calls(torch, [graph.replay], reps, 3, stream, "timed_drafter_pair")
+    hg.hg_sync(hd)
+    hg.hg_sync(ht)
+    for s_ in range(min(nd, 100)):
+        check_concat(torch, sd[s_], od[s_], TP, f"drafter set {s_}")
+    for s_ in range(min(nt, 100)):
+        check_concat(torch, st_[s_], ot[s_], TP, f"target set {s_}")
+    pair_graph = round(ms * 1000.0 / (reps * 100), 3)
+    del graph, pair_calls
+    # the same steps issued one by one from Python (direct-call objects)
+    fns = []
+    for i in range(max(nd, nt)):
+        fns.append(cd[i % nd])
+        fns.append(ct[i % nt])
+    ms_e = time_calls(torch, fns, 2 * steps, 2 * warmup, stream, "timed_drafter_pair_eager")
+    hg.hg_sync(hd)
+    hg.hg_sync(ht)
+    pair_eager = round(ms_e * 1000.0 / steps, 3)
+    # each handle alone, replayed from graphs
+    alone = {}
+    for name, h, sh_, ou_, n_, M in (("drafter", hd, sd, od, nd, DRAFT_M),
+                                     ("target", ht, st_, ot, nt, TARGET_M)):
+        k = [0]
+
+        def issue(h=h, sh_=sh_, ou_=ou_, n_=n_, M=M, k=k):
+            # on the current stream: the capture stream while the graph is taken
+            i = k[0] % n_
+            k[0] += 1
+            hg.hg_gather(h, [sh_[i, r] for r in range(TP)], [ou_[i, d] for d in range(TP)], M)
+        alone[name] = graph_us_per_launch(torch, issue, stream, label=f"timed_{name}_alone")
+        hg.hg_sync(h)
+    hd.close()
+    ht.close()
+    return {"drafter": {"tp": TP, "shard_cols": W, "rows": [1, 2, 3, 4], "M": DRAFT_M},
+            "target": {"tp": TP, "shard_cols": W, "rows": [1, 2, 3, 4, 5, 8], "M": TARGET_M},
+            "pair_us_per_step_graph_replay": pair_graph,
+            "pair_us_per_step_eager": pair_eager,
+            "drafter_alone_us": alone["drafter"], "target_alone_us": alone["target"],
+            "sum_alone_us": round(alone["drafter"] + alone["target"], 3)}
 
 
 # --------------------------------------------------------------------- ours --
@@ -526,6 +688,17 @@ def run_ours(args):
         graph_us = graph_replay_us(torch, hg, synth, TP, W, CAP, M_STEP, device, stream,
                                    args.steps, autotune=tune)
 
+    # ---- row statistics replayed from CUDA graphs, as the plain gather ----
+    stats_graph = {}
+    if not args.quick:
+        for M in (1, 4, 8):
+            stats_graph[str(M)] = stats_graph_us(torch, hg, synth, M, device, stream)
+
+    # ---- the drafter's gather beside the target's, on one stream ----
+    drafter = None
+    if not args.quick:
+        drafter = drafter_pair(torch, hg, synth, device, stream, args.warmup)
+
     # ---- e2e: pinned host buffers through hg_gather_host (the kernel reads the
     # shards from host memory and writes the outputs into host memory over the
     # host-device link), rotating over as many sets as the device workload ----
@@ -609,6 +782,19 @@ def run_ours(args):
             per_m_graph_tuned[str(M)] = graph_replay_us(
                 torch, hg, synth, TP, W, CAP, M, device, stream, 1000, rows=[M], seed=2,
                 autotune=True)
+    # ---- latency floors at the launch shapes of M = 1..8 (fixed rule) ----
+    floors = {}
+    hfl = hg.hg_create(TP, W, CAP)
+    shapes = {str(M): (hg.hg_launch_shape(hfl, M)["ctas"], 32 * TP)
+              for M in (range(1, 9) if not args.quick else [M_STEP])}
+    hfl.close()
+    floors = latency_floors(torch, hg, shapes, stream, device)
+    for M, f in floors.items():
+        g = per_m_graph.get(M) if M != str(M_STEP) else round(us_call, 3)
+        if g:
+            f["gather_us"] = g
+            f["gather_over_handoff"] = round(g / f["handoff_us"], 3)
+
     large = {}
     for M in ([] if args.quick else [64, 128, 256]):
         hm, sm_, om_, cm_ = make_workload(torch, hg, synth, TP, W, M, M, 3, device, rows=[M],
@@ -693,7 +879,13 @@ def run_ours(args):
                      "traffic": traffic,
                      "note": f"algorithmic bytes M*V*2*(1+4*TP) = {B} per launch; peak is the "
                              f"{pk['source']} HBM copy bandwidth; at M=1 the working set is "
-                             "L2-resident and the launch is latency-bound"},
+                             "L2-resident and the launch is latency-bound: latency_floor_us is "
+                             "the one-vector push->poll->copy->re-arm handoff kernel launched "
+                             "like the gather (same grid, graph-replayed)",
+                     "latency_floor_us": floors[str(M_STEP)]["handoff_us"],
+                     "empty_launch_us": floors[str(M_STEP)]["empty_launch_us"],
+                     "floor_multiple": round(us_launch / floors[str(M_STEP)]["handoff_us"], 3)},
+        "latency_floors_per_m": floors,
         "eager_us_per_call": round(eager_us, 3),
         "per_m": per_m,
         "per_m_launch": per_m_shape,
@@ -703,6 +895,8 @@ def run_ours(args):
         "per_m_graph_replay_autotuned": per_m_graph_tuned,
         "large_m": large,
         "with_row_stats_us_per_call": stats_us,
+        "with_row_stats_graph_replay": stats_graph,
+        "drafter_pair": drafter,
         "gather_then_torch_row_stats_us_per_call": torch_stats_us,
         "device_parity_us_per_call": devpar_us,
         "graph_replay_us_per_call": graph_us,
@@ -826,6 +1020,96 @@ def run_sweep(args):
     return 0
 
 
+def timeline_summary(rec, tp: int, grid: int) -> dict:
+    """Launch-by-launch figures of a timeline [calls, ctas, slots] (int64 ns,
+    calls in call order): when each launch's first and last CTA started, when
+    its wait for the previous kernel returned (first and last CTA), and when
+    its last warp finished."""
+    import numpy as np
+    r = rec[:, :grid, :]
+    entry = r[:, :, 0]
+    waited = r[:, :, 1]
+    cta_end = r[:, :, 2:2 + tp].max(axis=2)
+    e_min, e_max = entry.min(axis=1), entry.max(axis=1)
+    w_min, w_max = waited.min(axis=1), waited.max(axis=1)
+    end = cta_end.max(axis=1)
+    n = r.shape[0]
+    period = np.diff(w_min)                   # wait release to wait release
+    gap = w_min[1:] - end[:-1]                # previous kernel's last warp -> next wait release
+    span = end - w_min                        # first wait release -> last warp
+    early = (entry[1:] < end[:-1, None]).mean(axis=1)  # CTAs resident before the previous ended
+    ser = end - e_min                         # first CTA start -> last warp (what a serialised
+                                              # launch would take from its first CTA)
+
+    def st(x):
+        return {"mean": round(float(x.mean()) / 1000, 3), "median": round(float(np.median(x)) / 1000, 3),
+                "p10": round(float(np.percentile(x, 10)) / 1000, 3),
+                "p90": round(float(np.percentile(x, 90)) / 1000, 3)}
+    return {"launches": n, "ctas": grid,
+            "period_us": st(period), "exposed_gap_us": st(gap), "span_after_wait_us": st(span),
+            "first_to_last_cta_wait_us": st(w_max - w_min),
+            "first_cta_start_to_last_warp_us": st(ser),
+            "first_cta_start_before_wait_release_us": st(w_min - e_min),
+            "cta_end_median_after_wait_us": st(np.median(cta_end, axis=1) - w_min),
+            "share_of_ctas_resident_before_previous_ended": round(float(early.mean()), 3),
+            "total_us_first_wait_to_last_end": round(float(end[-1] - w_min[0]) / 1000, 3)}
+
+
+def run_timeline(args):
+    """Timeline of back-to-back graph-replayed gathers (TP8, V=163840, cap 8)
+    from the measurement build (hg_options.timeline_calls): one JSON line per
+    M with the launch-by-launch figures, beside the per-call time of the same
+    graph replayed without the timeline build."""
+    import torch
+
+    from tp_vocab_logits_gb300 import _build, hg, synth
+    _build.build()
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    for M in [int(x) for x in args.timeline_ms.split(",")]:
+        n = sets_for(TP, W, M)
+        res = {}
+        for tl in (200, 0):
+            h, sh, ou, calls = make_workload(torch, hg, synth, TP, W, CAP, M, n, device,
+                                             rows=[M], seed=2, device_parity=True,
+                                             timeline_calls=tl)
+            stats = hg.new_row_stats(M) if args.timeline_stats else None
+            k = [0]
+
+            def issue():
+                i = k[0] % n
+                k[0] += 1
+                if stats is not None:
+                    hg.hg_gather_stats(h, [sh[i, r] for r in range(TP)],
+                                       [ou[i, d] for d in range(TP)], stats, M)
+                else:
+                    hg.hg_gather(h, [sh[i, r] for r in range(TP)], [ou[i, d] for d in range(TP)],
+                                 M)
+            issue()
+            hg.hg_sync(h)
+            us = graph_us_per_launch(torch, issue, stream, reps=5,
+                                     label=f"timed_timeline_m{M}_{tl}")
+            hg.hg_sync(h)
+            check_concat(torch, sh[0], ou[0], TP, f"timeline M={M}")
+            if tl:
+                rec, nxt = hg.hg_timeline(h)
+                rec = rec.cpu().numpy()
+                import numpy as np
+                rec = np.concatenate([rec[nxt:], rec[:nxt]])  # call order
+                grid = hg.hg_launch_shape(h, M)["ctas"] if stats is None else \
+                    int((rec[0, :, 0] > 0).sum())
+                res = timeline_summary(rec, TP, grid)
+                res["graph_replay_us_per_call_timeline_build"] = us
+            else:
+                res["graph_replay_us_per_call"] = us
+            h.close()
+            del sh, ou, calls
+        print(json.dumps(dict(res, timeline="gather" if not args.timeline_stats else
+                              "gather_stats", tp=TP, shard_cols=W, M=M)), flush=True)
+    return 0
+
+
 def run_stats_only(args):
     """hg_gather_stats on the step workload (TP8, V=163840, cap 8, M rows),
     one JSON line per M: us/call, checked against the plain gather's outputs."""
@@ -897,6 +1181,12 @@ def main(argv=None):
     ap.add_argument("--stats", action="store_true",
                     help="hg_gather_stats only (TP8, V=163840), one line per M")
     ap.add_argument("--stats-ms", default="1,4,8")
+    ap.add_argument("--timeline", action="store_true",
+                    help="launch timeline of graph-replayed gathers (TP8, V=163840), one line "
+                         "per M")
+    ap.add_argument("--timeline-ms", default="1,8")
+    ap.add_argument("--timeline-stats", action="store_true",
+                    help="--timeline: time hg_gather_stats instead of hg_gather")
     ap.add_argument("--fused-w", type=int, default=20480, help="fused: shard columns per rank")
     ap.add_argument("--tps", default="2,4,8,16")
     ap.add_argument("--widths", default="4096,8192,20480,65536")
@@ -922,6 +1212,8 @@ def main(argv=None):
         return run_fused_only(args)
     if args.stats:
         return run_stats_only(args)
+    if args.timeline:
+        return run_timeline(args)
     return run_ours(args)
 
 

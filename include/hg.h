@@ -103,6 +103,14 @@ typedef struct hg_options {
                                rule. It costs
                                tens of milliseconds per served row count at the
                                decode sizes and changes no result, only speed */
+  int timeline_calls;       /* 0 (default): off; n > 0: a measurement build of
+                               the gather records, for each of the last n
+                               calls of hg_gather and hg_gather_stats, per CTA
+                               when it started, when its wait for the previous
+                               kernel returned and when each warp finished
+                               (hg_timeline). Needs shard_cols % 8 == 0,
+                               tp <= 16 and no prefetch; it costs a few stores
+                               per CTA and changes no result */
 } hg_options;
 
 /*
@@ -236,6 +244,56 @@ int hg_mailbox(const hg_handle *h, int rank, const void **dev_ptr, size_t *bytes
  * gather_ctas(m, ...) in HeadGather.__init__, is named but not printed. */
 int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *elems_per_lane,
                     int *prefetch);
+
+/* One CTA's record in the timeline of hg_options.timeline_calls: %globaltimer
+ * nanoseconds at entry (before the kernel waits for the previous kernel on
+ * the stream), once that wait returned, and when warp d finished (d < tp;
+ * warps of CTAs that gave up record nothing). */
+#define HG_TIMELINE_SLOTS 18
+typedef struct hg_timeline_record {
+  uint64_t entry;
+  uint64_t waited;
+  uint64_t warp_done[HG_TIMELINE_SLOTS - 2];
+} hg_timeline_record;
+
+/*
+ * hg_timeline - the timeline of a handle created with timeline_calls = n:
+ * device pointer to [n][ctas] hg_timeline_record (ctas = the largest grid of
+ * any served row count; a call of a smaller grid fills its first CTAs), and
+ * the index of the record the next call writes (calls fill records 0, 1, ...
+ * in call order and wrap around after n). Read it only while no gather of the
+ * handle is in flight. A measurement surface with no counterpart on the
+ * pages. Errors: HG_ERR_ARG (NULL, or a handle without a timeline).
+ */
+int hg_timeline(const hg_handle *h, const hg_timeline_record **dev_ptr, int *calls, int *ctas,
+                int *next);
+
+/*
+ * hg_probe - measurement kernels that bound the gather's latency from below;
+ * no counterpart on the pages. Both are launched as the gather is (a
+ * programmatic dependent launch of `ctas` CTAs of `threads` threads, a
+ * multiple of 32, at most 512) on `stream`:
+ *
+ *   kind 0  empty: wait for the previous kernel, let the next one launch,
+ *           return. The cost of one dependent launch of that grid.
+ *   kind 1  handoff: warp w of CTA g stores one 16-byte vector per lane into
+ *           its slot, lets the next kernel launch, polls the slot of CTA
+ *           g + 1 (mod ctas) until it arrives (relaxed loads, bounded by 1 s),
+ *           stores it to an output and re-arms that slot: the gather's push,
+ *           poll, copy and re-arm for one vector per lane and no shard read.
+ *
+ *   scratch  device buffer of hg_probe_scratch_bytes(ctas, threads) bytes,
+ *            16-byte aligned, owned by the caller; kind 1 needs it armed by
+ *            kind 2 (fill the slots with the sentinel, clear the status word)
+ *            once before its first launch, and leaves it armed; the status
+ *            word (the last 4 bytes) becomes 1 if a poll gave up.
+ *
+ * Errors: HG_ERR_ARG (kind, sizes, NULL or misaligned scratch), HG_ERR_CUDA.
+ */
+int hg_probe(int kind, int ctas, int threads, void *scratch, hg_stream_t stream);
+
+/* Bytes of the scratch buffer of hg_probe for that grid. */
+size_t hg_probe_scratch_bytes(int ctas, int threads);
 
 /*
  * Test hook for failure detection: make rank `rank`'s push skip its rows in

@@ -60,6 +60,13 @@ def test_host_checks_without_device(lib):
     c = ctypes.c_int()
     assert lib.hg_launch_shape(None, 1, ctypes.byref(c), None, None, None) == hg.HG_ERR_ARG
     assert lib.hg_stock_gather(0, 8, None, None, 1, None) == hg.HG_ERR_ARG
+    p = ctypes.c_void_p()
+    assert lib.hg_timeline(None, ctypes.byref(p), None, None, None) == hg.HG_ERR_ARG
+    for kind, ctas, threads in [(3, 1, 32), (-1, 1, 32), (0, 0, 32), (0, 1, 33), (0, 1, 1024)]:
+        assert lib.hg_probe(kind, ctas, threads, None, None) == hg.HG_ERR_ARG
+    assert lib.hg_probe(1, 4, 64, None, None) == hg.HG_ERR_ARG   # scratch needed
+    assert lib.hg_probe_scratch_bytes(4, 64) == 2 * 4 * 64 * 16 + 16
+    assert lib.hg_probe_scratch_bytes(0, 64) == 0
     for code in range(7):
         assert lib.hg_strerror(code)
     assert lib.hg_strerror(99) == b"unknown status"

@@ -379,9 +379,13 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
 // issued one iteration ahead. MAXT: largest CTA (32 * tp). STATS: warp 0
 // (rank 0's copy of every row) also folds each consumed unit into a
 // statistics cell, and warp 0 of CTA g folds the cells of rows g, g + G, ...
-template <typename V, int VPT, bool PREF, int MAXT, bool STATS>
+// TL: the kernel records when each CTA starts, passes the wait and when each
+// of its warps finishes (a measurement build; the others record nothing).
+template <typename V, int VPT, bool PREF, int MAXT, bool STATS, bool TL = false>
 __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
+  unsigned long long tl_entry = 0;
+  if constexpr (TL) tl_entry = globaltimer_ns();
   const int lane = (int)threadIdx.x & 31;
   const int d = (int)threadIdx.x >> 5;  // this warp's rank: mailbox and output
   const int N = a.M * a.tp * a.chunks;  // units
@@ -425,6 +429,13 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   // stream has completed and its memory is visible. Apart from the L2
   // prefetch, nothing reads or writes global memory before the wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (TL) {
+    if (threadIdx.x == 0) {
+      unsigned long long* rec = a.timeline + (size_t)blockIdx.x * kTimelineSlots;
+      rec[0] = tl_entry;
+      rec[1] = globaltimer_ns();
+    }
+  }
 
   // The first push's shard loads do not depend on the parity: start them
   // before anything else, so that their latency overlaps the parity and
@@ -517,6 +528,9 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   // TP8 V=163840 at 3 elements per lane (216 cells) in one wait; wider units
   // leave fewer cells and fewer free registers.
   if (STATS && d == 0 && g < a.M) finish_stats<(VPT <= 4 ? 8 : 6)>(a, g, G);
+  if constexpr (TL) {
+    if (lane == 0) a.timeline[(size_t)g * kTimelineSlots + 2 + d] = globaltimer_ns();
+  }
 }
 
 __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
@@ -528,6 +542,20 @@ __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
 // Kernels for tp <= 16 (CTAs of up to 512 threads) take 1 to 6 elements per
 // lane; larger tp (up to 1024 threads, 64 registers) 1 or 2. Row statistics
 // exist for tp <= 16.
+// Timeline builds: 16-byte vectors, no prefetch, tp <= 16.
+template <bool STATS>
+const void* pick_timeline(int vpt) {
+  switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&gather_kernel<uint4, 1, false, 512, STATS, true>);
+    case 2: return reinterpret_cast<const void*>(&gather_kernel<uint4, 2, false, 512, STATS, true>);
+    case 3: return reinterpret_cast<const void*>(&gather_kernel<uint4, 3, false, 512, STATS, true>);
+    case 4: return reinterpret_cast<const void*>(&gather_kernel<uint4, 4, false, 512, STATS, true>);
+    case 5: return reinterpret_cast<const void*>(&gather_kernel<uint4, 5, false, 512, STATS, true>);
+    case 6: return reinterpret_cast<const void*>(&gather_kernel<uint4, 6, false, 512, STATS, true>);
+    default: return nullptr;
+  }
+}
+
 template <typename V, bool PREF, bool STATS>
 const void* pick_vpt(int vpt, int tp) {
   if (tp <= 16) {
@@ -555,6 +583,10 @@ const void* pick_stats(const LaunchShape& s, int tp) {
 }
 
 const void* kernel_for(const LaunchShape& s, bool vec16, int tp) {
+  if (s.timeline) {
+    if (!vec16 || s.pref || tp > 16) return nullptr;
+    return s.stats ? pick_timeline<true>(s.vpt) : pick_timeline<false>(s.vpt);
+  }
   if (vec16) return s.pref ? pick_stats<uint4, true>(s, tp) : pick_stats<uint4, false>(s, tp);
   return s.pref ? pick_stats<uint32_t, true>(s, tp) : pick_stats<uint32_t, false>(s, tp);
 }

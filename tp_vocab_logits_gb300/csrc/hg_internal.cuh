@@ -67,7 +67,16 @@ struct GatherArgs {
   // 1: before waiting on the previous kernel, each CTA prefetches its first
   // push unit of the shards into L2 (shards in device memory only).
   int l2_prefetch = 0;
+  // Timeline record of this call (kernels built with it only): CTA g writes
+  // %globaltimer readings into timeline[g * kTimelineSlots + k]: k = 0 at
+  // entry, 1 once the wait for the previous kernel has returned, 2 + d when
+  // warp d has finished (the statistics reducer included).
+  unsigned long long* timeline = nullptr;
 };
+
+// 64-bit slots of one CTA's timeline record (entry, after the wait, one end
+// time per warp for up to 16 warps).
+constexpr int kTimelineSlots = 2 + 16;
 
 // Launch shape of one row count: CTAs (32 * tp threads each), elements per lane
 // per unit, and whether the next push's shard loads are issued one iteration
@@ -78,6 +87,8 @@ struct LaunchShape {
   bool pref = false;
   bool stats = false;  // the kernel also folds row statistics
   bool late = false;   // trigger the next launch late (see trigger_late)
+  bool timeline = false;  // the kernel writes a timeline record (16-byte vector
+                          // path, tp <= 16, no prefetch)
 };
 
 // The kernel indexes units with int: a CTA's push index t * G + g runs up to

@@ -45,6 +45,10 @@ struct hg_handle {
   uint32_t* split_cells = nullptr;  // fused calls: split cells of the tail tiles (armed)
   size_t split_cell_count = 0;
   int max_ctas = 0;                 // hg_options.ctas: also caps the fused grid
+  unsigned long long* timeline = nullptr;  // [timeline_calls][timeline_ctas] records
+  int timeline_calls = 0;
+  int timeline_ctas = 0;
+  long long timeline_next = 0;      // calls recorded so far
 };
 
 namespace {
@@ -63,6 +67,7 @@ void free_handle(hg_handle* h) {
   if (h->parity_words) cudaFree(h->parity_words);
   if (h->partials) cudaFree(h->partials);
   if (h->split_cells) cudaFree(h->split_cells);
+  if (h->timeline) cudaFree(h->timeline);
   delete h;
 }
 
@@ -74,6 +79,9 @@ int check_shape_options(const hg_handle* h, const hg_options* opt) {
       opt->prefetch > 2)
     return HG_ERR_ARG;
   if (opt->autotune < 0 || opt->autotune > 1) return HG_ERR_ARG;
+  if (opt->timeline_calls < 0) return HG_ERR_ARG;
+  if (opt->timeline_calls > 0 && (!h->vec16 || h->tp > 16 || opt->prefetch == 1))
+    return HG_ERR_ARG;
   return HG_OK;
 }
 
@@ -261,6 +269,36 @@ int hg_create_ex(int tp, int shard_cols, int cap, const int* rows, int nrows,
     st = autotune_shapes(h, opt);
     if (st != HG_OK) { free_handle(h); return st; }
   }
+  if (opt && opt->timeline_calls > 0) {
+    // Timeline records: the measurement build of the kernel (no prefetch; the
+    // tuner may have chosen it, so it is switched off for these shapes). Its
+    // grid must stay co-resident with the measurement build's own occupancy.
+    int max_ctas = 0;
+    for (int M = 1; M <= cap; ++M) {
+      if (!h->served[M]) continue;
+      for (int k = 0; k < 2; ++k) {
+        hg::LaunchShape& sh = k == 0 ? h->shape[M] : h->shape_stats[M];
+        const int chunks = k == 0 ? h->chunks[M] : h->chunks_stats[M];
+        sh.pref = false;
+        sh.timeline = true;
+        long long maxg = 0;
+        st = max_grid(h, sh, &maxg);
+        if (st != HG_OK) { free_handle(h); return st; }
+        if (sh.ctas > maxg) sh.ctas = (int)maxg;
+        sh.late = hg::trigger_late(sh.ctas, (long long)M * tp * chunks, maxg);
+        max_ctas = std::max(max_ctas, sh.ctas);
+      }
+    }
+    h->timeline_calls = opt->timeline_calls;
+    h->timeline_ctas = max_ctas;
+    const size_t bytes = (size_t)h->timeline_calls * max_ctas * hg::kTimelineSlots * 8;
+    if (cudaMalloc(&h->timeline, bytes) != cudaSuccess ||
+        cudaMemset(h->timeline, 0, bytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+      free_handle(h);
+      return HG_ERR_CUDA;
+    }
+  }
   if (h->device_parity) {
     // One copy per reader: warp d of CTA g of a gather reads copy g * tp + d,
     // CTA g of a fused call (at most one CTA per SM) reads copy g.
@@ -346,8 +384,12 @@ int gather_impl(hg_handle* h, const void* const* shard_ptrs, void* const* out_pt
     a.shard_cols = h->W;
   }
   const hg::LaunchShape& shape = stats ? h->shape_stats[M] : h->shape[M];
+  if (h->timeline)
+    a.timeline = h->timeline + (size_t)(h->timeline_next % h->timeline_calls) *
+                                   h->timeline_ctas * hg::kTimelineSlots;
   if (hg::launch_gather(a, shape, h->vec16, stream, h->cooperative) != cudaSuccess)
     return HG_ERR_CUDA;
+  if (h->timeline) ++h->timeline_next;
   if (!h->device_parity) h->parity ^= 1;
   return HG_OK;
 }
@@ -659,6 +701,17 @@ int hg_launch_shape(const hg_handle* h, int M, int* ctas, int* threads, int* ele
   if (threads) *threads = 32 * h->tp;
   if (elems_per_lane) *elems_per_lane = s.vpt;
   if (prefetch) *prefetch = s.pref ? 1 : 0;
+  return HG_OK;
+}
+
+int hg_timeline(const hg_handle* h, const hg_timeline_record** dev_ptr, int* calls, int* ctas,
+                int* next) {
+  static_assert(sizeof(hg_timeline_record) == hg::kTimelineSlots * 8, "timeline record layout");
+  if (!h || !h->timeline || !dev_ptr) return HG_ERR_ARG;
+  *dev_ptr = reinterpret_cast<const hg_timeline_record*>(h->timeline);
+  if (calls) *calls = h->timeline_calls;
+  if (ctas) *ctas = h->timeline_ctas;
+  if (next) *next = (int)(h->timeline_next % h->timeline_calls);
   return HG_OK;
 }
 

@@ -30,7 +30,8 @@ class HGError(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("poll_timeout_ns", ctypes.c_uint64), ("elems_per_lane", ctypes.c_int),
                 ("ctas", ctypes.c_int), ("prefetch", ctypes.c_int), ("cooperative", ctypes.c_int),
-                ("device_parity", ctypes.c_int), ("autotune", ctypes.c_int)]
+                ("device_parity", ctypes.c_int), ("autotune", ctypes.c_int),
+                ("timeline_calls", ctypes.c_int)]
 
 
 _LIB: ctypes.CDLL | None = None
@@ -66,12 +67,17 @@ def load() -> ctypes.CDLL:
     lib.hg_stock_gather.argtypes = [i, i, vpp, vpp, i, st]
     lib.hg_gather_fused.argtypes = [vp, vpp, vpp, vpp, vpp, i, i, st]
     lib.hg_gather_stats.argtypes = [vp, vpp, vpp, i, vp, st]
+    lib.hg_timeline.argtypes = [vp, ctypes.POINTER(vp), ip, ip, ip]
+    lib.hg_probe.argtypes = [i, i, i, vp, st]
+    lib.hg_probe_scratch_bytes.argtypes = [i, i]
+    lib.hg_probe_scratch_bytes.restype = ctypes.c_size_t
     lib.hg_strerror.argtypes = [i]
     lib.hg_strerror.restype = ctypes.c_char_p
     for name in ("hg_create", "hg_create_ex", "hg_destroy", "hg_gather", "hg_gather_host",
                  "hg_sync", "hg_rearm",
                  "hg_parity", "hg_mailbox", "hg_launch_shape", "hg_debug_skip_push",
-                 "hg_stock_gather", "hg_gather_fused", "hg_gather_stats"):
+                 "hg_stock_gather", "hg_gather_fused", "hg_gather_stats", "hg_timeline",
+                 "hg_probe"):
         getattr(lib, name).restype = i
     _LIB = lib
     return lib
@@ -126,15 +132,16 @@ class Handle:
 def hg_create(tp: int, shard_cols: int, cap: int, rows: Sequence[int] | None = None, *,
               poll_timeout_ns: int = 0, elems_per_lane: int = 0, ctas: int = 0,
               prefetch: int = 0, cooperative: bool = False,
-              device_parity: bool = False, autotune: bool = False) -> Handle:
+              device_parity: bool = False, autotune: bool = False,
+              timeline_calls: int = 0) -> Handle:
     lib = load()
     rows = list(rows or [])
     arr = (ctypes.c_int * max(1, len(rows)))(*rows)
     out = ctypes.c_void_p()
     if poll_timeout_ns or elems_per_lane or ctas or prefetch or cooperative or device_parity \
-            or autotune:
+            or autotune or timeline_calls:
         opt = _Options(poll_timeout_ns, elems_per_lane, ctas, prefetch, int(bool(cooperative)),
-                       int(bool(device_parity)), int(bool(autotune)))
+                       int(bool(device_parity)), int(bool(autotune)), int(timeline_calls))
         st = lib.hg_create_ex(tp, shard_cols, cap, arr, len(rows), ctypes.byref(opt),
                               ctypes.byref(out))
     else:
@@ -308,6 +315,42 @@ def hg_launch_shape(h: Handle, M: int) -> dict:
                                   ctypes.byref(p)), "hg_launch_shape")
     return {"ctas": c.value, "threads": t.value, "elems_per_lane": e.value,
             "prefetch": bool(p.value)}
+
+
+TIMELINE_SLOTS = 18  # HG_TIMELINE_SLOTS: entry, after the wait, one end time per warp
+
+
+def hg_timeline(h: Handle) -> tuple:
+    """(records, next): a copy of the handle's timeline as an int64 device
+    tensor [calls, ctas, TIMELINE_SLOTS] of %globaltimer nanoseconds (slot 0
+    entry, 1 after the wait, 2 + d when warp d finished), and the index of the
+    record the next call writes. Read it only while no gather is in flight."""
+    p = ctypes.c_void_p()
+    calls, ctas, nxt = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load().hg_timeline(h.ptr, ctypes.byref(p), ctypes.byref(calls), ctypes.byref(ctas),
+                              ctypes.byref(nxt)), "hg_timeline")
+    shape = (calls.value, ctas.value, TIMELINE_SLOTS)
+    view = torch.as_tensor(_DeviceView(int(p.value), shape, "<i8"), device="cuda")
+    return view.clone(), nxt.value
+
+
+def hg_probe_scratch_bytes(ctas: int, threads: int) -> int:
+    return int(load().hg_probe_scratch_bytes(ctas, threads))
+
+
+def hg_probe(kind: int, ctas: int, threads: int, scratch: torch.Tensor | None = None,
+             stream=None) -> None:
+    """Measurement kernels launched as the gather is (see include/hg.h):
+    kind 0 empty dependent launch, 1 one-vector push/poll/copy/re-arm
+    handoff, 2 arm the handoff's scratch (a device tensor of at least
+    hg_probe_scratch_bytes(ctas, threads) bytes)."""
+    ptr = None
+    if scratch is not None:
+        if not scratch.is_cuda or scratch.numel() * scratch.element_size() < \
+                hg_probe_scratch_bytes(ctas, threads):
+            raise ValueError("scratch: need a CUDA tensor of hg_probe_scratch_bytes bytes")
+        ptr = scratch.data_ptr()
+    _check(load().hg_probe(kind, ctas, threads, ptr, _stream_ptr(stream)), "hg_probe")
 
 
 def hg_debug_skip_push(h: Handle, rank: int) -> None:
