@@ -1097,6 +1097,8 @@ def run_timeline(args):
                 rec = rec.cpu().numpy()
                 import numpy as np
                 rec = np.concatenate([rec[nxt:], rec[:nxt]])  # call order
+                if args.timeline_dump:  # the first 50 launches
+                    np.save(f"{args.timeline_dump}_m{M}.npy", rec[:50])
                 grid = hg.hg_launch_shape(h, M)["ctas"] if stats is None else \
                     int((rec[0, :, 0] > 0).sum())
                 res = timeline_summary(rec, TP, grid)
@@ -1185,6 +1187,8 @@ def main(argv=None):
                     help="launch timeline of graph-replayed gathers (TP8, V=163840), one line "
                          "per M")
     ap.add_argument("--timeline-ms", default="1,8")
+    ap.add_argument("--timeline-dump", default="",
+                    help="--timeline: also save the raw records to <prefix>_m<M>.npy")
     ap.add_argument("--timeline-stats", action="store_true",
                     help="--timeline: time hg_gather_stats instead of hg_gather")
     ap.add_argument("--fused-w", type=int, default=20480, help="fused: shard columns per rank")

@@ -172,7 +172,9 @@ __device__ __forceinline__ void issue_polls(const V* box, const UnitPos& p, unsi
 // Poll this lane's elements of unit u in mailbox `box` until none holds a
 // sentinel word; res receives the data. A lane that waits too long (or sees an
 // error raised elsewhere) gives up; the warp leaves together (vote). Returns
-// false when the warp gave up.
+// false when the warp gave up. The status word is loaded together with each
+// round of re-polls and looked at in the next round, so that a retry costs
+// one memory round trip, not two.
 template <typename V, int VPT>
 __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, const UnitPos& p,
                                           int u, int d, V (&res)[VPT]) {
@@ -182,6 +184,7 @@ __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, con
     if (p.idx + 32 * v < a.wv) todo |= 1u << v;
   unsigned long long t_wait = 0;
   bool gave_up = false;
+  int status = kDevOk;  // as loaded with the previous round of polls
   issue_polls<V, VPT>(box, p, todo, res);
   for (;;) {
 #pragma unroll
@@ -190,7 +193,7 @@ __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, con
     if (todo) {
       const unsigned long long now = globaltimer_ns();
       if (t_wait == 0) t_wait = now;
-      if (now - t_wait > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+      if (now - t_wait > a.timeout_ns || status != kDevOk) {
         record_timeout(a, u, d, p.dst);
         gave_up = true;
         todo = 0;
@@ -198,81 +201,112 @@ __device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, con
     }
     if (__all_sync(kFull, todo == 0)) break;
     issue_polls<V, VPT>(box, p, todo, res);
+    status = ld_relaxed_s32(a.status);
   }
   return !__any_sync(kFull, gave_up);
 }
 
 // ---- Row statistics (max, first argmax, sum of exp(x - max)) -------------
+//
+// Every step here is branch-free (comparisons feed selects, never jumps): a
+// per-value condition that diverges inside a warp costs tens of cycles of
+// divergence handling, and a fold touches 24 values per lane. A warp's
+// result comes from each lane's own (max, first argmax, sum of exp(x - lane
+// max)), then one warp max (redux.sync on an order-preserving key), one warp
+// min over the lanes that hold that max (the first argmax), and a shuffle sum
+// of the lanes' sums rescaled to the warp max.
 
 constexpr float kNegInf = -__builtin_huge_valf();
+constexpr int kNoColumn = 0x7fffffff;
 
-// (mx, arg) <- the larger of (mx, arg) and (x, col); ties keep the smaller column.
-__device__ __forceinline__ void max_add(float& mx, int& arg, float x, int col) {
-  if (x > mx || (x == mx && col < arg)) {
-    mx = x;
-    arg = col;
-  }
+// Unsigned key of a float whose unsigned order is the float order (-0 below
+// +0; NaNs at the ends), and back.
+__device__ __forceinline__ unsigned order_key(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // (mx, arg, s) <- its combination with (mx2, arg2, s2), where s is a sum of
-// exp(x - mx) over finite x (0 when mx is -inf).
+// exp(x - mx) over finite x (0 when mx is -inf); ties keep the smaller
+// column. Both exponentials are taken before the selects.
 __device__ __forceinline__ void combine_partial(float& mx, int& arg, float& s, float mx2,
                                                 int arg2, float s2) {
   const float m = fmaxf(mx, mx2);
   const int a = mx > mx2 ? arg : (mx2 > mx ? arg2 : min(arg, arg2));
-  float t = 0.f;
-  if (mx != kNegInf) t += s * __expf(mx - m);
-  if (mx2 != kNegInf) t += s2 * __expf(mx2 - m);
+  const float e1 = __expf(mx - m);
+  const float e2 = __expf(mx2 - m);
+  const float t1 = mx != kNegInf ? s * e1 : 0.f;
+  const float t2 = mx2 != kNegInf ? s2 * e2 : 0.f;
   mx = m;
   arg = a;
+  s = t1 + t2;
+}
+
+// Warp-wide (max, first argmax, sum of exp(x - max)) from every lane's own
+// (lane_mx, lane_arg, lane_s), lane_s relative to lane_mx; every lane
+// receives the result.
+__device__ __forceinline__ void warp_stats(float lane_mx, int lane_arg, float lane_s, float& mx,
+                                           int& arg, float& s) {
+  mx = key_float(__reduce_max_sync(kFull, order_key(lane_mx)));
+  const unsigned cand = lane_mx == mx ? (unsigned)lane_arg : (unsigned)kNoColumn;
+  arg = (int)__reduce_min_sync(kFull, cand);
+  const float e = __expf(lane_mx - mx);
+  float t = lane_mx != kNegInf ? lane_s * e : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(kFull, t, off);
   s = t;
 }
 
 // Statistics of unit u's values, folded by warp 0 from rank 0's copy (every
-// rank's copy holds the same values). Two passes over registers: the warp's
-// max and first argmax, then the sum of exp(x - max) over finite x. Lane 0
-// writes the result into cell u with one relaxed 16-byte store.
+// rank's copy holds the same values). Per lane: the max (a tree of fmaxf),
+// then in one pass the sum of exp(x - lane max) and the smallest column
+// holding the lane max; then warp_stats. Lane 0 writes the result into cell u
+// with one relaxed 16-byte store.
 template <typename V, int VPT>
 __device__ __forceinline__ void unit_stats(const GatherArgs& a, const UnitPos& p, int u,
                                            const V (&res)[VPT]) {
   using E = Elem<V>;
-  float mx = kNegInf;
-  int arg = 0x7fffffff;
+  // Pass 1: the lane max over the words (each word: the larger half), two
+  // interleaved chains of fmaxf. Words of a vector beyond the row count as
+  // two -inf values.
+  float m0 = kNegInf, m1 = kNegInf;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
-    if (p.idx + 32 * v < a.wv) {
-      const int col0 = p.r * a.shard_cols + (p.idx + 32 * v) * (2 * E::kWords);
+    const bool ok = p.idx + 32 * v < a.wv;
 #pragma unroll
-      for (int k = 0; k < E::kWords; ++k) {
-        const uint32_t w = E::word(res[v], k);
-        max_add(mx, arg, __uint_as_float(w << 16), col0 + 2 * k);
-        max_add(mx, arg, __uint_as_float(w & 0xffff0000u), col0 + 2 * k + 1);
-      }
+    for (int k = 0; k < E::kWords; ++k) {
+      const uint32_t w = E::word(res[v], k);
+      const float m = fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+      if ((v * E::kWords + k) & 1) m1 = fmaxf(m1, ok ? m : kNegInf);
+      else m0 = fmaxf(m0, ok ? m : kNegInf);
     }
   }
+  const float lm = fmaxf(m0, m1);
+  // Pass 2, from the words again: the sum of exp(x - lane max) and the
+  // smallest column holding the lane max.
+  int la = kNoColumn;
+  float ls = 0.f;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float m2 = __shfl_xor_sync(kFull, mx, off);
-    const int a2 = __shfl_xor_sync(kFull, arg, off);
-    max_add(mx, arg, m2, a2);
-  }
-  float s = 0.f;
-  if (mx != kNegInf) {
+  for (int v = 0; v < VPT; ++v) {
+    const bool ok = p.idx + 32 * v < a.wv;
+    const int col0 = p.r * a.shard_cols + (p.idx + 32 * v) * (2 * E::kWords);
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      if (p.idx + 32 * v < a.wv) {
-#pragma unroll
-        for (int k = 0; k < E::kWords; ++k) {
-          const uint32_t w = E::word(res[v], k);
-          const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-          if (lo != kNegInf) s += __expf(lo - mx);
-          if (hi != kNegInf) s += __expf(hi - mx);
-        }
-      }
+    for (int k = 0; k < E::kWords; ++k) {
+      const uint32_t w = E::word(res[v], k);
+      const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+      const float e = __expf(lo - lm) + __expf(hi - lm);  // exp(-inf) = 0; lm = -inf: below
+      ls += ok ? e : 0.f;
+      const int c = hi == lm ? col0 + 2 * k + 1 : kNoColumn;
+      la = ok ? min(la, lo == lm ? col0 + 2 * k : c) : la;
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  if (lm == kNegInf) ls = 0.f;
+  float mx, s;
+  int arg;
+  warp_stats(lm, la, ls, mx, arg, s);
   if ((threadIdx.x & 31) == 0) {
     // A Lamport cell: no word may equal the sentinel, so a -0.0 max is
     // written as +0.0 (the same value); the other words cannot be it.
@@ -301,7 +335,7 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
   for (int m = g; m < a.M; m += G) {
     uint4* q = reinterpret_cast<uint4*>(a.partials + (size_t)m * per_row);
     float mx = kNegInf, s = 0.f;
-    int arg = 0x7fffffff;
+    int arg = kNoColumn;
     bool gave_up = false;
     for (int base = lane; base < per_row && !gave_up; base += BATCH * 32) {
       // A batch of cells in flight; the ones still armed are re-loaded
@@ -317,6 +351,7 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
       }
       const unsigned valid = todo;
       unsigned long long t0 = 0;
+      int status = kDevOk;  // loaded with the previous round of polls
       for (;;) {
 #pragma unroll
         for (int k = 0; k < BATCH; ++k)
@@ -324,7 +359,7 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
         if (!todo) break;
         const unsigned long long now = globaltimer_ns();
         if (t0 == 0) t0 = now;
-        if (now - t0 > a.timeout_ns || ld_relaxed_s32(a.status) != kDevOk) {
+        if (now - t0 > a.timeout_ns || status != kDevOk) {
           record_timeout(a, -1, -1, (size_t)base);
           gave_up = true;
           break;
@@ -332,37 +367,37 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
 #pragma unroll
         for (int k = 0; k < BATCH; ++k)
           if (todo >> k & 1) v[k] = Elem<uint4>::ld_poll(q + base + 32 * k);
+        status = ld_relaxed_s32(a.status);
       }
       if (gave_up) break;
-      // The batch's max and first argmax, then its sum rescaled to that max:
-      // the exponentials are independent of one another.
-      float bm = kNegInf, bs = 0.f;
-      int ba = 0x7fffffff;
+      // The batch: its max (a tree), then in one pass its smallest column at
+      // that max and its sum rescaled to it (independent exponentials).
+      float km[BATCH];
 #pragma unroll
       for (int k = 0; k < BATCH; ++k)
-        if (valid >> k & 1) max_add(bm, ba, __uint_as_float(v[k].x), (int)v[k].y);
+        km[k] = (valid >> k & 1) ? __uint_as_float(v[k].x) : kNegInf;
+      float tm[BATCH];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) tm[k] = km[k];
+#pragma unroll
+      for (int step = 1; step < BATCH; step <<= 1)
+#pragma unroll
+        for (int k = 0; k + step < BATCH; k += 2 * step) tm[k] = fmaxf(tm[k], tm[k + step]);
+      const float bm = tm[0];
+      int ba = kNoColumn;
+      float bs = 0.f;
 #pragma unroll
       for (int k = 0; k < BATCH; ++k) {
-        if (!(valid >> k & 1)) continue;
-        const float ck = __uint_as_float(v[k].x);
-        if (ck != kNegInf) bs += __uint_as_float(v[k].z) * __expf(ck - bm);
-        Elem<uint4>::st_relaxed(q + base + 32 * k, armed);
+        const float e = __expf(km[k] - bm);
+        bs += (km[k] != kNegInf) ? __uint_as_float(v[k].z) * e : 0.f;
+        ba = ((valid >> k & 1) && km[k] == bm) ? min(ba, (int)v[k].y) : ba;
+        if (valid >> k & 1) Elem<uint4>::st_relaxed(q + base + 32 * k, armed);
       }
       combine_partial(mx, arg, s, bm, ba, bs);
     }
-    // Across the warp in the same two steps: max and first argmax, then the
-    // lanes' sums rescaled to it.
-    float rm = mx;
-    int ra = arg;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float m2 = __shfl_xor_sync(kFull, rm, off);
-      const int a2 = __shfl_xor_sync(kFull, ra, off);
-      max_add(rm, ra, m2, a2);
-    }
-    float rs = mx != kNegInf ? s * __expf(mx - rm) : 0.f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) rs += __shfl_xor_sync(kFull, rs, off);
+    float rm, rs;
+    int ra;
+    warp_stats(mx, arg, s, rm, ra, rs);
     if (__any_sync(kFull, gave_up)) return;
     if (lane == 0) {
       hg_row_stats r;
@@ -382,7 +417,8 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
 // TL: the kernel records when each CTA starts, passes the wait and when each
 // of its warps finishes (a measurement build; the others record nothing).
 template <typename V, int VPT, bool PREF, int MAXT, bool STATS, bool TL = false>
-__global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
+__global__ void __launch_bounds__(MAXT, (STATS && MAXT == 512) ? 2 : 1)
+    gather_kernel(const __grid_constant__ GatherArgs a) {
   using E = Elem<V>;
   unsigned long long tl_entry = 0;
   if constexpr (TL) tl_entry = globaltimer_ns();
@@ -501,6 +537,12 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
       const UnitPos p = unit_pos<VPT>(a, uc, lane);
       V res[VPT];
       if (!poll_unit<V, VPT>(a, box, p, uc, d, res)) return;
+      // Statistics timeline (tp <= 8: the slots of warps 8..10): when warp 0's
+      // poll of its latest unit completed, its stores were issued, its fold
+      // was stored.
+      constexpr bool kTlStats = TL && STATS;
+      const bool tl_here = kTlStats && d == 0 && lane == 0 && a.tp <= 8;
+      if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 8] = globaltimer_ns();
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
         if (p.idx + 32 * v < a.wv) {
@@ -508,8 +550,10 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
           E::st_relaxed(box + p.dst + 32 * v, E::sentinel());
         }
       }
+      if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 9] = globaltimer_ns();
       // After the stores, so that the folding overlaps their completion.
       if (STATS && d == 0) unit_stats<V, VPT>(a, p, uc, res);
+      if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 10] = globaltimer_ns();
     }
   }
   if (a.late_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -527,6 +571,12 @@ __global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ Ga
   // Warp 0 of CTA g: rows g, g + G, ... Eight cells per lane cover a row of
   // TP8 V=163840 at 3 elements per lane (216 cells) in one wait; wider units
   // leave fewer cells and fewer free registers.
+  if constexpr (TL && STATS) {
+    // When warp 0 turns to the statistics reducer (the slot of warp 15,
+    // which a statistics CTA of tp <= 15 warps does not have).
+    if (d == 0 && lane == 0 && a.tp < 16)
+      a.timeline[(size_t)g * kTimelineSlots + 2 + 15] = globaltimer_ns();
+  }
   if (STATS && d == 0 && g < a.M) finish_stats<(VPT <= 4 ? 8 : 6)>(a, g, G);
   if constexpr (TL) {
     if (lane == 0) a.timeline[(size_t)g * kTimelineSlots + 2 + d] = globaltimer_ns();
