@@ -260,8 +260,8 @@ __device__ __forceinline__ void warp_stats(float lane_mx, int lane_arg, float la
   s = t;
 }
 
-// Statistics of unit u's values, folded by warp 0 from rank 0's copy (every
-// rank's copy holds the same values). Per lane: the max (a tree of fmaxf),
+// Statistics of unit u's values, folded by one warp from its rank's copy
+// (every rank's copy holds the same values). Per lane: the max (a tree of fmaxf),
 // then in one pass the sum of exp(x - lane max) and the smallest column
 // holding the lane max; then warp_stats. Lane 0 writes the result into cell u
 // with one relaxed 16-byte store.
@@ -411,14 +411,14 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
 }
 
 // VPT: elements per lane per unit. PREF: the next push's shard loads are
-// issued one iteration ahead. MAXT: largest CTA (32 * tp). STATS: warp 0
-// (rank 0's copy of every row) also folds each consumed unit into a
-// statistics cell, and warp 0 of CTA g folds the cells of rows g, g + G, ...
+// issued one iteration ahead. MAXT: largest CTA (32 * tp). STATS: one warp
+// also folds each consumed unit into a statistics cell (the unit of
+// iteration t: warp (t - 1) mod tp), and warp 0 of CTA g folds the cells of
+// rows g, g + G, ...
 // TL: the kernel records when each CTA starts, passes the wait and when each
 // of its warps finishes (a measurement build; the others record nothing).
-template <typename V, int VPT, bool PREF, int MAXT, bool STATS, bool TL = false>
-__global__ void __launch_bounds__(MAXT, (STATS && MAXT == 512) ? 2 : 1)
-    gather_kernel(const __grid_constant__ GatherArgs a) {
+template <typename V, int VPT, bool PREF, int MAXT, bool STATS, bool TL>
+__device__ __forceinline__ void gather_body(const GatherArgs& a) {
   using E = Elem<V>;
   unsigned long long tl_entry = 0;
   if constexpr (TL) tl_entry = globaltimer_ns();
@@ -537,11 +537,11 @@ __global__ void __launch_bounds__(MAXT, (STATS && MAXT == 512) ? 2 : 1)
       const UnitPos p = unit_pos<VPT>(a, uc, lane);
       V res[VPT];
       if (!poll_unit<V, VPT>(a, box, p, uc, d, res)) return;
-      // Statistics timeline (tp <= 8: the slots of warps 8..10): when warp 0's
-      // poll of its latest unit completed, its stores were issued, its fold
-      // was stored.
+      // Statistics timeline (tp <= 8: the slots of warps 8..10): when the
+      // folding warp's poll of the CTA's latest unit completed, its stores
+      // were issued, its fold was stored.
       constexpr bool kTlStats = TL && STATS;
-      const bool tl_here = kTlStats && d == 0 && lane == 0 && a.tp <= 8;
+      const bool tl_here = kTlStats && d == (t - 1) % a.tp && lane == 0 && a.tp <= 8;
       if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 8] = globaltimer_ns();
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
@@ -552,7 +552,10 @@ __global__ void __launch_bounds__(MAXT, (STATS && MAXT == 512) ? 2 : 1)
       }
       if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 9] = globaltimer_ns();
       // After the stores, so that the folding overlaps their completion.
-      if (STATS && d == 0) unit_stats<V, VPT>(a, p, uc, res);
+      // Every warp holds the same values (its rank's copy of the unit): the
+      // fold of iteration t goes to warp (t - 1) mod tp, so that no warp
+      // falls behind the others by one fold per iteration.
+      if (STATS && d == (t - 1) % a.tp) unit_stats<V, VPT>(a, p, uc, res);
       if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 10] = globaltimer_ns();
     }
   }
@@ -583,6 +586,21 @@ __global__ void __launch_bounds__(MAXT, (STATS && MAXT == 512) ? 2 : 1)
   }
 }
 
+// The gather: register use left to the compiler under the CTA-size bound
+// (54 and 62 registers at 3 and 4 vectors per lane: 4 CTAs of 256 threads
+// per SM).
+template <typename V, int VPT, bool PREF, int MAXT, bool TL = false>
+__global__ void __launch_bounds__(MAXT) gather_kernel(const __grid_constant__ GatherArgs a) {
+  gather_body<V, VPT, PREF, MAXT, false, TL>(a);
+}
+
+// The gather with row statistics (tp <= 16): held to 64 registers, so that 4
+// CTAs of 256 threads fit per SM as for the plain gather.
+template <typename V, int VPT, bool PREF, bool TL = false>
+__global__ void __launch_bounds__(512, 2) gather_stats_kernel(const __grid_constant__ GatherArgs a) {
+  gather_body<V, VPT, PREF, 512, true, TL>(a);
+}
+
 __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x)
@@ -592,37 +610,39 @@ __global__ void fill_u32_kernel(uint32_t* p, size_t n, uint32_t v) {
 // Kernels for tp <= 16 (CTAs of up to 512 threads) take 1 to 6 elements per
 // lane; larger tp (up to 1024 threads, 64 registers) 1 or 2. Row statistics
 // exist for tp <= 16.
-// Timeline builds: 16-byte vectors, no prefetch, tp <= 16.
-template <bool STATS>
-const void* pick_timeline(int vpt) {
+// Kernel of elements per lane VPT for a template pattern: the gather or the
+// gather with statistics, with or without the timeline.
+template <typename V, bool PREF, bool STATS, bool TL, int VPT>
+const void* kernel_ptr() {
+  if constexpr (STATS)
+    return reinterpret_cast<const void*>(&gather_stats_kernel<V, VPT, PREF, TL>);
+  else
+    return reinterpret_cast<const void*>(&gather_kernel<V, VPT, PREF, 512, TL>);
+}
+
+template <typename V, bool PREF, bool STATS, bool TL>
+const void* pick_512(int vpt) {
   switch (vpt) {
-    case 1: return reinterpret_cast<const void*>(&gather_kernel<uint4, 1, false, 512, STATS, true>);
-    case 2: return reinterpret_cast<const void*>(&gather_kernel<uint4, 2, false, 512, STATS, true>);
-    case 3: return reinterpret_cast<const void*>(&gather_kernel<uint4, 3, false, 512, STATS, true>);
-    case 4: return reinterpret_cast<const void*>(&gather_kernel<uint4, 4, false, 512, STATS, true>);
-    case 5: return reinterpret_cast<const void*>(&gather_kernel<uint4, 5, false, 512, STATS, true>);
-    case 6: return reinterpret_cast<const void*>(&gather_kernel<uint4, 6, false, 512, STATS, true>);
+    case 1: return kernel_ptr<V, PREF, STATS, TL, 1>();
+    case 2: return kernel_ptr<V, PREF, STATS, TL, 2>();
+    case 3: return kernel_ptr<V, PREF, STATS, TL, 3>();
+    case 4: return kernel_ptr<V, PREF, STATS, TL, 4>();
+    case 5: return kernel_ptr<V, PREF, STATS, TL, 5>();
+    case 6: return kernel_ptr<V, PREF, STATS, TL, 6>();
     default: return nullptr;
   }
 }
 
+// Kernels for tp <= 16 (CTAs of up to 512 threads) take 1 to 6 elements per
+// lane; larger tp (up to 1024 threads, 64 registers) 1 or 2. Row statistics
+// exist for tp <= 16; timeline builds for 16-byte vectors without prefetch.
 template <typename V, bool PREF, bool STATS>
 const void* pick_vpt(int vpt, int tp) {
-  if (tp <= 16) {
-    switch (vpt) {
-      case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PREF, 512, STATS>);
-      case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PREF, 512, STATS>);
-      case 3: return reinterpret_cast<const void*>(&gather_kernel<V, 3, PREF, 512, STATS>);
-      case 4: return reinterpret_cast<const void*>(&gather_kernel<V, 4, PREF, 512, STATS>);
-      case 5: return reinterpret_cast<const void*>(&gather_kernel<V, 5, PREF, 512, STATS>);
-      case 6: return reinterpret_cast<const void*>(&gather_kernel<V, 6, PREF, 512, STATS>);
-      default: return nullptr;
-    }
-  }
+  if (tp <= 16) return pick_512<V, PREF, STATS, false>(vpt);
   if (STATS) return nullptr;
   switch (vpt) {
-    case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PREF, 1024, false>);
-    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PREF, 1024, false>);
+    case 1: return reinterpret_cast<const void*>(&gather_kernel<V, 1, PREF, 1024>);
+    case 2: return reinterpret_cast<const void*>(&gather_kernel<V, 2, PREF, 1024>);
     default: return nullptr;
   }
 }
@@ -635,7 +655,8 @@ const void* pick_stats(const LaunchShape& s, int tp) {
 const void* kernel_for(const LaunchShape& s, bool vec16, int tp) {
   if (s.timeline) {
     if (!vec16 || s.pref || tp > 16) return nullptr;
-    return s.stats ? pick_timeline<true>(s.vpt) : pick_timeline<false>(s.vpt);
+    return s.stats ? pick_512<uint4, false, true, true>(s.vpt)
+                   : pick_512<uint4, false, false, true>(s.vpt);
   }
   if (vec16) return s.pref ? pick_stats<uint4, true>(s, tp) : pick_stats<uint4, false>(s, tp);
   return s.pref ? pick_stats<uint32_t, true>(s, tp) : pick_stats<uint32_t, false>(s, tp);
