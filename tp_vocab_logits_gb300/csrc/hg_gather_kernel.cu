@@ -170,22 +170,30 @@ __device__ __forceinline__ void issue_polls(const V* box, const UnitPos& p, unsi
 }
 
 // Poll this lane's elements of unit u in mailbox `box` until none holds a
-// sentinel word; res receives the data. A lane that waits too long (or sees an
-// error raised elsewhere) gives up; the warp leaves together (vote). Returns
-// false when the warp gave up. The status word is loaded together with each
-// round of re-polls and looked at in the next round, so that a retry costs
-// one memory round trip, not two.
+// sentinel word; res receives the data. poll_begin issues the first loads
+// (so that other work can overlap their round trip); poll_finish waits. A
+// lane that waits too long (or sees an error raised elsewhere) gives up; the
+// warp leaves together (vote). poll_finish returns false when the warp gave
+// up. The status word is loaded together with each round of re-polls and
+// looked at in the next round, so that a retry costs one memory round trip,
+// not two.
 template <typename V, int VPT>
-__device__ __forceinline__ bool poll_unit(const GatherArgs& a, const V* box, const UnitPos& p,
-                                          int u, int d, V (&res)[VPT]) {
+__device__ __forceinline__ unsigned poll_begin(const GatherArgs& a, const V* box,
+                                               const UnitPos& p, V (&res)[VPT]) {
   unsigned todo = 0;  // bit v: slot v still waits
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
     if (p.idx + 32 * v < a.wv) todo |= 1u << v;
+  issue_polls<V, VPT>(box, p, todo, res);
+  return todo;
+}
+
+template <typename V, int VPT>
+__device__ __forceinline__ bool poll_finish(const GatherArgs& a, const V* box, const UnitPos& p,
+                                            int u, int d, unsigned todo, V (&res)[VPT]) {
   unsigned long long t_wait = 0;
   bool gave_up = false;
   int status = kDevOk;  // as loaded with the previous round of polls
-  issue_polls<V, VPT>(box, p, todo, res);
   for (;;) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
@@ -412,9 +420,9 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
 
 // VPT: elements per lane per unit. PREF: the next push's shard loads are
 // issued one iteration ahead. MAXT: largest CTA (32 * tp). STATS: one warp
-// also folds each consumed unit into a statistics cell (the unit of
-// iteration t: warp (t - 1) mod tp), and warp 0 of CTA g folds the cells of
-// rows g, g + G, ...
+// also folds each pushed unit into a statistics cell (the push of iteration
+// t: warp t mod tp), and warp 0 of CTA g folds the cells of rows g, g + G,
+// ...
 // TL: the kernel records when each CTA starts, passes the wait and when each
 // of its warps finishes (a measurement build; the others record nothing).
 template <typename V, int VPT, bool PREF, int MAXT, bool STATS, bool TL>
@@ -530,18 +538,31 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
 #pragma unroll
       for (int v = 0; v < VPT; ++v)
         if (pn.idx + 32 * v < a.wv) E::st_relaxed(box + pn.dst + 32 * v, E::rewrite(xn[v]));
+      // Statistics are folded where the values already sit in registers: at
+      // the push. Every warp pushes the same unit (into its own rank's
+      // mailbox), so the fold of iteration t's push goes to warp t mod tp and
+      // no warp falls behind by one fold per iteration. The values are the
+      // shard's own words: a sentinel word (+0, -0) that the push sends as
+      // (+0, +0) holds the same two values to every comparison, sum and exp.
+      if (STATS && d == t % a.tp) unit_stats<V, VPT>(a, pn, t * G + g, xn);
     }
     if (PREF) load_push(t + 1);
     const int uc = (t - 1) * G + cons;
     if (uc < N) {
       const UnitPos p = unit_pos<VPT>(a, uc, lane);
       V res[VPT];
-      if (!poll_unit<V, VPT>(a, box, p, uc, d, res)) return;
-      // Statistics timeline (tp <= 8: the slots of warps 8..10): when the
-      // folding warp's poll of the CTA's latest unit completed, its stores
-      // were issued, its fold was stored.
+      const unsigned todo = poll_begin<V, VPT>(a, box, p, res);
+      // Statistics timeline (tp <= 8: the slots of warps 8..10): when warp 0
+      // had folded iteration 0's push, its first poll completed and its stores
+      // were issued.
       constexpr bool kTlStats = TL && STATS;
-      const bool tl_here = kTlStats && d == (t - 1) % a.tp && lane == 0 && a.tp <= 8;
+      const bool tl_here = kTlStats && t == 1 && d == 0 && lane == 0 && a.tp <= 8;
+      // Iteration 0's push is folded by warp 0 while its first polls travel
+      // (every CTA consumes in iteration 1: cons < G <= N).
+      if (STATS && t == 1 && d == 0 && push0 && p0.r != a.skip_rank)
+        unit_stats<V, VPT>(a, p0, g, x0);
+      if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 10] = globaltimer_ns();
+      if (!poll_finish<V, VPT>(a, box, p, uc, d, todo, res)) return;
       if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 8] = globaltimer_ns();
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
@@ -551,12 +572,6 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
         }
       }
       if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 9] = globaltimer_ns();
-      // After the stores, so that the folding overlaps their completion.
-      // Every warp holds the same values (its rank's copy of the unit): the
-      // fold of iteration t goes to warp (t - 1) mod tp, so that no warp
-      // falls behind the others by one fold per iteration.
-      if (STATS && d == (t - 1) % a.tp) unit_stats<V, VPT>(a, p, uc, res);
-      if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 10] = globaltimer_ns();
     }
   }
   if (a.late_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
