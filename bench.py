@@ -381,6 +381,18 @@ def graph_us_per_launch(torch, issue, stream, n_graph=200, reps=5, label="timed_
     return round(ms * 1000.0 / (reps * n_graph), 3)
 
 
+def l2_copy_gbs(torch, device, stream, mib: int = 24, reps: int = 200) -> float:
+    """Bandwidth of a device copy whose source and destination (2 x `mib` MiB)
+    stay resident in L2, read + write bytes over CUDA-event time: the rate the
+    decode-size gather's L2-resident traffic could reach at best."""
+    n = mib * 2**20 // 2
+    a = torch.ones(n, dtype=torch.int16, device=device)
+    b = torch.empty_like(a)
+    ms = time_calls(torch, [lambda: b.copy_(a)], reps, 20, stream, "timed_l2_copy")
+    del a, b
+    return round(2 * n * 2 * reps / (ms * 1e-3) / 1e9, 1)
+
+
 def latency_floors(torch, hg, shapes, stream, device) -> dict:
     """The two floor kernels of hg_probe at each launch shape {key: (ctas,
     threads)}: an empty dependent launch, and the one-vector push -> poll ->
@@ -789,11 +801,16 @@ def run_ours(args):
               for M in (range(1, 9) if not args.quick else [M_STEP])}
     hfl.close()
     floors = latency_floors(torch, hg, shapes, stream, device)
+    l2_gbs = l2_copy_gbs(torch, device, stream)
     for M, f in floors.items():
         g = per_m_graph.get(M) if M != str(M_STEP) else round(us_call, 3)
         if g:
             f["gather_us"] = g
             f["gather_over_handoff"] = round(g / f["handoff_us"], 3)
+            # algorithmic bytes at the L2-resident copy rate: a bandwidth bound
+            bound = algorithmic_bytes(TP, W, int(M)) / (l2_gbs * 1e9) * 1e6
+            f["l2_copy_bound_us"] = round(bound, 3)
+            f["frac_of_l2_copy"] = round(bound / g, 3)
 
     large = {}
     for M in ([] if args.quick else [64, 128, 256]):
@@ -886,6 +903,7 @@ def run_ours(args):
                      "empty_launch_us": floors[str(M_STEP)]["empty_launch_us"],
                      "floor_multiple": round(us_launch / floors[str(M_STEP)]["handoff_us"], 3)},
         "latency_floors_per_m": floors,
+        "l2_copy_GBps": l2_gbs,
         "eager_us_per_call": round(eager_us, 3),
         "per_m": per_m,
         "per_m_launch": per_m_shape,
