@@ -1130,6 +1130,63 @@ def run_timeline(args):
     return 0
 
 
+def run_fused_timeline(args):
+    """Timeline of back-to-back fused calls (TP8, V=163840, K=7168) at each M:
+    per launch, when the CTAs started, finished set-up, pushed each item,
+    consumed the neighbour's items and finished (hg_gather_fused records in the
+    handle's timeline). One JSON line per M; raw records with --timeline-dump."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from tp_vocab_logits_gb300 import _build, hg, synth
+    _build.build()
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    tp, K, Wd, n = 8, 7168, 20480, 12
+    weight = [synth.weight(4, r, Wd, K, device=device) for r in range(tp)]
+    lib = hg.load()
+    wp = (ctypes.c_void_p * tp)(*[w.data_ptr() for w in weight])
+    for M in [int(x) for x in args.timeline_ms.split(",")]:
+        h = hg.hg_create(tp, Wd, 8, rows=[1, 4, 8], timeline_calls=n)
+        hid = synth.hidden(4, tp, M, K, device=device)
+        outs = torch.empty((tp, M, tp * Wd), dtype=torch.int16, device=device)
+        hp = (ctypes.c_void_p * tp)(*[hid[r].data_ptr() for r in range(tp)])
+        op = (ctypes.c_void_p * tp)(*[outs[d].data_ptr() for d in range(tp)])
+        for _ in range(n):
+            st = lib.hg_gather_fused(h.ptr, hp, wp, None, op, M, K, stream.cuda_stream)
+            if st != 0:
+                raise SystemExit(f"hg_gather_fused failed: {hg.strerror(st)}")
+        hg.hg_sync(h)
+        rec, nxt = hg.hg_timeline(h)
+        rec = rec.cpu().numpy()
+        rec = np.concatenate([rec[nxt:], rec[:nxt]])  # call order
+        G = int((rec[0, :, 0] > 0).sum())
+        r = rec[:, :G, :]
+        if args.timeline_dump:
+            np.save(f"{args.timeline_dump}_fused_m{M}.npy", r)
+        e0 = r[:, :, 0].min(axis=1)
+
+        def rel(x):
+            return (x - e0[:, None]) / 1000.0
+        done = rel(r[:, :, 17])
+        out = {"fused_timeline": True, "M": M, "ctas": G, "calls": n,
+               "period_us": round(float(np.median(np.diff(e0))) / 1000, 3),
+               "setup_done_us": round(float(np.median(rel(r[:, :, 1]))), 3),
+               "push_item_us_median": [round(float(np.median(rel(r[:, :, 2 + i]))), 2)
+                                       for i in range(8)],
+               "consume_item_us_median": [round(float(np.median(rel(r[:, :, 10 + j]))), 2)
+                                          for j in range(6)],
+               "loop_done_us": [round(float(np.percentile(rel(r[:, :, 16]), q)), 2)
+                                for q in (0, 50, 100)],
+               "cta_done_us": [round(float(np.percentile(done, q)), 2) for q in (0, 50, 100)]}
+        print(json.dumps(out), flush=True)
+        h.close()
+    return 0
+
+
 def run_stats_only(args):
     """hg_gather_stats on the step workload (TP8, V=163840, cap 8, M rows),
     one JSON line per M: us/call, checked against the plain gather's outputs."""
@@ -1205,6 +1262,9 @@ def main(argv=None):
                     help="launch timeline of graph-replayed gathers (TP8, V=163840), one line "
                          "per M")
     ap.add_argument("--timeline-ms", default="1,8")
+    ap.add_argument("--fused-timeline", action="store_true",
+                    help="launch timeline of back-to-back fused calls (TP8, K=7168), one line "
+                         "per M of --timeline-ms")
     ap.add_argument("--timeline-dump", default="",
                     help="--timeline: also save the raw records to <prefix>_m<M>.npy")
     ap.add_argument("--timeline-stats", action="store_true",
@@ -1236,6 +1296,8 @@ def main(argv=None):
         return run_stats_only(args)
     if args.timeline:
         return run_timeline(args)
+    if args.fused_timeline:
+        return run_fused_timeline(args)
     return run_ours(args)
 
 

@@ -105,10 +105,10 @@ typedef struct hg_options {
                                decode sizes and changes no result, only speed */
   int timeline_calls;       /* 0 (default): off; n > 0: a measurement build of
                                the gather records, for each of the last n
-                               calls of hg_gather and hg_gather_stats, per CTA
-                               when it started, when its wait for the previous
-                               kernel returned and when each warp finished
-                               (hg_timeline). Needs shard_cols % 8 == 0,
+                               calls of hg_gather, hg_gather_stats and
+                               hg_gather_fused, per CTA when it started, when
+                               its wait for the previous kernel returned and
+                               when each warp finished (hg_timeline). Needs shard_cols % 8 == 0,
                                tp <= 16 and no prefetch; it costs a few stores
                                per CTA and changes no result */
 } hg_options;
@@ -250,7 +250,13 @@ int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *ele
  * the stream), once that wait returned, and when warp d finished (d < tp;
  * warps of CTAs that gave up record nothing). In hg_gather_stats calls with
  * tp < 16, warp_done[15] holds when warp 0 finished its share of the gather
- * and turned to reducing the statistics of its rows. */
+ * and turned to reducing the statistics of its rows. hg_gather_fused calls
+ * (one CTA per SM; recorded when the handle's grid records have room for it)
+ * use the same slots differently: entry; set-up done (tensor memory and
+ * barriers ready); warp_done[i] (i < 8): the epilogue has pushed its item i;
+ * warp_done[8 + j] (j < 6): it has consumed the neighbour CTA's item j inside
+ * its loop; warp_done[14]: the epilogue loop is done; warp_done[15]: the CTA
+ * is done. */
 #define HG_TIMELINE_SLOTS 18
 typedef struct hg_timeline_record {
   uint64_t entry;

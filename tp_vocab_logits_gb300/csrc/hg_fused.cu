@@ -225,6 +225,14 @@ __device__ __forceinline__ void st_relaxed_v4(uint4* p, uint4 v) {
                : "memory");
 }
 
+// Output store, evict-first: the caller reads the outputs once, and the L2 is
+// better spent on the mailboxes (as in the gather kernel).
+__device__ __forceinline__ void st_out_v4(uint4* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ bool arrived_v4(uint4 v) {
   return v.x != kSentinel && v.y != kSentinel && v.z != kSentinel && v.w != kSentinel;
 }
@@ -360,7 +368,7 @@ __device__ bool consume_tile(const FusedArgs& a, int it, size_t parity_off, int 
           }
         } while (true);
       }
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.out[d]) + off) = x[k];
+      st_out_v4(reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.out[d]) + off), x[k]);
       st_relaxed_v4(p, sent);
     }
   }
@@ -378,6 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
 
   const int warp = (int)threadIdx.x >> 5;
   const int lane = (int)threadIdx.x & 31;
+  // Timeline record (measurement only): slots of this CTA, written by one thread.
+  unsigned long long* const tl =
+      a.timeline ? a.timeline + (size_t)blockIdx.x * kTimelineSlots : nullptr;
+  if (tl && threadIdx.x == 0) tl[kFusedTlEntry] = globaltimer_ns();
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // Device-resident parity: this CTA's copy g (every thread reads it; the CTA
@@ -410,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
+  if (tl && threadIdx.x == 0) tl[kFusedTlSetup] = globaltimer_ns();
 
   const int G = (int)gridDim.x;
   const int g = (int)blockIdx.x;
@@ -584,14 +597,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
           }
         }
       }  // whole tile or part 0
+      if (tl && warp == 2 && lane == 0 && i < kFusedTlPushN) tl[kFusedTlPush + i] = globaltimer_ns();
       // One item behind, the gather of the neighbour's tiles: its item i - 1
       // was pushed about one tile of weight streaming ago, so these polls
       // rarely wait, and the copy overlaps this CTA's next tile.
       if (i >= 1 && i - 1 < n_cons) {
         const bool ok = consume_tile(a, cons_tile(i - 1), parity_off, (int)threadIdx.x - 64, 128);
         if (!__all_sync(0xffffffffu, ok)) break;
+        if (tl && warp == 2 && lane == 0 && i - 1 < kFusedTlConsumeN)
+          tl[kFusedTlConsume + i - 1] = globaltimer_ns();
       }
     }
+    if (tl && warp == 2 && lane == 0) tl[kFusedTlLoopDone] = globaltimer_ns();
   }
 
   // All roles done (or stopped on an error): free the tensor memory. One
@@ -626,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   // consumed (its last one or two), by every thread.
   for (int k = n_items >= 1 ? n_items - 1 : 0; k < n_cons; ++k)
     if (!consume_tile(a, cons_tile(k), parity_off, (int)threadIdx.x, kThreads)) return;
+  if (tl && threadIdx.x == 0) tl[kFusedTlDone] = globaltimer_ns();
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -702,6 +720,7 @@ cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   a.parity_entries = l.parity_entries;
   a.parity_stride_words = l.parity_stride_words;
   a.skip_rank = l.skip_rank;
+  a.timeline = nullptr;
   a.tp = l.tp;
   a.W = l.W;
   a.K = l.K;
@@ -715,6 +734,7 @@ cudaError_t fused_launch(const FusedLaunch& l, cudaStream_t stream, int sms) {
   int grid = sms * per_sm;
   if (l.max_ctas > 0 && grid > l.max_ctas) grid = l.max_ctas;
   if (grid > items) grid = items;
+  if (l.timeline && grid <= l.timeline_ctas) a.timeline = l.timeline;
   // Work split: whole tiles in full waves; a tail of at most half the grid is
   // split along K (at most kMaxSplit parts, each of at least one K block) if
   // the handle has split cells for it.

@@ -173,7 +173,18 @@ struct FusedArgs {
   int split;
   uint32_t* split_cells;
   int skip_rank;  // test hook: rank whose mailbox pushes are skipped (-1: none)
+  // Timeline record of this call (nullptr: none): CTA g writes %globaltimer
+  // readings into timeline[g * kTimelineSlots + k] (see kFusedTl*).
+  unsigned long long* timeline;
 };
+
+// Slots of a fused call's timeline record per CTA: entry, set-up done (TMEM
+// allocated, barriers ready), item i pushed by the epilogue (i < 8), the
+// neighbour's item j consumed inside the epilogue loop (j < 6), the
+// epilogue loop done, the CTA done.
+constexpr int kFusedTlEntry = 0, kFusedTlSetup = 1, kFusedTlPush = 2, kFusedTlPushN = 8,
+              kFusedTlConsume = 10, kFusedTlConsumeN = 6, kFusedTlLoopDone = 16,
+              kFusedTlDone = 17;
 
 // Armed word of a split cell, and the word a partial with that bit pattern
 // is written as (both NaNs).
@@ -201,6 +212,8 @@ struct FusedLaunch {
   size_t split_cell_count = 0;      // cells available (each kSplitCellWords words)
   int max_ctas = 0;                 // cap on the grid (0: one CTA per SM)
   int skip_rank = -1;               // test hook: rank whose pushes are skipped
+  unsigned long long* timeline = nullptr;  // record of this call (nullptr: none)
+  int timeline_ctas = 0;                   // CTAs the record has room for
 };
 
 // Limits of the fused path: TP, rows, K granularity, W granularity.

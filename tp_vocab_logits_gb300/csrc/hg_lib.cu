@@ -767,7 +767,13 @@ int hg_gather_fused(hg_handle* h, const void* const* hidden_ptrs, const void* co
   l.split_cell_count = h->split_cell_count;
   l.max_ctas = h->max_ctas;
   l.skip_rank = h->skip_rank;
+  if (h->timeline) {
+    l.timeline = h->timeline + (size_t)(h->timeline_next % h->timeline_calls) *
+                                   h->timeline_ctas * hg::kTimelineSlots;
+    l.timeline_ctas = h->timeline_ctas;
+  }
   if (hg::fused::fused_launch(l, stream, h->sms) != cudaSuccess) return HG_ERR_CUDA;
+  if (h->timeline) ++h->timeline_next;
   if (!h->device_parity) h->parity ^= 1;
   return HG_OK;
 }
