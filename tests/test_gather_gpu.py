@@ -434,7 +434,7 @@ def test_create_rejects_bad_sizes():
     with pytest.raises(hg.HGError):
         hg.hg_create(24, 64, 4, elems_per_lane=3)  # 1024-thread CTAs: 1 or 2 per lane
     h = hg.hg_create(8, 20480, 8)
-    assert [hg.hg_launch_shape(h, M)["elems_per_lane"] for M in (1, 2, 3, 8)] == [3, 3, 4, 4]
+    assert [hg.hg_launch_shape(h, M)["elems_per_lane"] for M in (1, 2, 3, 4, 8)] == [3, 3, 3, 4, 4]
     h.close()
     h = hg.hg_create(16, 4096, 2)
     assert hg.hg_launch_shape(h, 1)["elems_per_lane"] == 4

@@ -96,7 +96,7 @@ int max_grid(const hg_handle* h, const hg::LaunchShape& s, long long* g) {
 
 // Launch shape for M rows by the fixed rule, unless the options force part of
 // it: one CTA = one warp per virtual rank; each lane carries default_vpt(tp, M)
-// elements (3 for one or two rows at tp <= 8, 4 otherwise, 2 for CTAs of 1024
+// elements (3 for up to three rows at tp <= 8, 4 otherwise, 2 for CTAs of 1024
 // threads; the statistics kernel: stats_vpt); one CTA per unit up to the
 // co-resident maximum, beyond which the CTAs loop over the units; no prefetch.
 // The best shape depends on tp, W and M in ways no simple rule captures, so
