@@ -248,7 +248,8 @@ int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *ele
 /* One CTA's record in the timeline of hg_options.timeline_calls: %globaltimer
  * nanoseconds at entry (before the kernel waits for the previous kernel on
  * the stream), once that wait returned, and when warp d finished (d < tp;
- * warps of CTAs that gave up record nothing). In hg_gather_stats calls with
+ * warps of CTAs that gave up record nothing); for tp <= 14, warp_done[14]
+ * holds instead the index of the SM the CTA ran on. In hg_gather_stats calls with
  * tp < 16, warp_done[15] holds when warp 0 finished its share of the gather
  * and turned to reducing the statistics of its rows. hg_gather_fused calls
  * (one CTA per SM; recorded when the handle's grid records have room for it)

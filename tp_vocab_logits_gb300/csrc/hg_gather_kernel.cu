@@ -478,6 +478,13 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
       unsigned long long* rec = a.timeline + (size_t)blockIdx.x * kTimelineSlots;
       rec[0] = tl_entry;
       rec[1] = globaltimer_ns();
+      // The SM this CTA runs on, in the slot of warp 14 (a CTA of tp <= 14
+      // warps has none).
+      if (a.tp <= 14) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        rec[2 + 14] = smid;
+      }
     }
   }
 
