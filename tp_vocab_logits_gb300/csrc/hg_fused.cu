@@ -23,8 +23,8 @@
 // tile overlaps the MMAs of the next). Warp 0 is the TMA producer, warp 1 the
 // MMA issuer (and owner of the TMEM allocation), warps 2..5 the epilogue: each
 // reads its 32 TMEM lanes (= 32 vocab rows) with tcgen05.ld, rounds to bf16,
-// packs column pairs into 32-bit words, rewrites the sentinel and stores the
-// word into all TP mailboxes. The GEMM streams each weight byte from HBM once
+// packs column pairs into 32-bit words, stages them in shared memory, and
+// stores them as 16-byte vectors, sentinel rewritten, into all TP mailboxes. The GEMM streams each weight byte from HBM once
 // (evict-first), so the kernel is bound by HBM bandwidth on the weights.
 //
 // Tail split. Tiles are dealt round-robin to the CTAs (one CTA per SM, all
@@ -73,7 +73,11 @@ constexpr int kAccCols = 16;     // fp32 columns of one accumulator
 constexpr uint32_t kTmemCols = 32;  // two accumulators (power of two >= 32)
 constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kPollBatch = 8;    // gather phase: mailbox vectors per thread in flight
-constexpr size_t kSmemBytes = (size_t)kStages * (kABytes + kBBytes) + 1024 /*align*/ + 256;
+// Per epilogue warp, its [16 rows m][16 words] of packed logits, staged so that
+// the push moves 16-byte vectors.
+constexpr size_t kStageWordsPerWarp = (size_t)kMmaN * 16;
+constexpr size_t kSmemBytes = (size_t)kStages * (kABytes + kBBytes) + 1024 /*align*/ + 256 +
+                              4 * kStageWordsPerWarp * sizeof(uint32_t);
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), A and B K-major (bits 15,
@@ -204,10 +208,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t w;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
   return w;
-}
-
-__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint4 ld_poll_v4(const uint4* p) {
@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   unsigned char* sA = base;
   unsigned char* sB = base + (size_t)kStages * kABytes;
   Shared* sh = reinterpret_cast<Shared*>(sB + (size_t)kStages * kBBytes);
+  uint32_t* const stage_words = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(sh) + 256);
 
   const int warp = (int)threadIdx.x >> 5;
   const int lane = (int)threadIdx.x & 31;
@@ -577,25 +578,57 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
 
         const int r = w.tile / a.tiles_per_rank;
         const int t = w.tile - r * a.tiles_per_rank;
-        // Word of vocab columns (row, row + 1) of rank r, for even rows.
-        const size_t wcol = (size_t)t * (kTileN / 2) + (size_t)(row >> 1);
         uint32_t* lg = reinterpret_cast<uint32_t*>(a.logits[r]);
+        // Pack column pairs (row, row + 1) into words (low half = even column) and
+        // stage the warp's [M][16] words (its 32 vocab rows) in shared memory:
+        // then lane l takes row m = l / 4 (and m + 8) and the 4 words, 8 vocab
+        // rows, of group l % 4, and pushes them as one 16-byte vector per rank
+        // instead of one 4-byte word per rank from every other lane.
+        uint32_t* const stage = stage_words + (size_t)(warp - 2) * kStageWordsPerWarp;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
           if (m < a.M) {
             const float mine = __uint_as_float(v[m]);
             const float next = __shfl_down_sync(0xffffffffu, mine, 1);
-            if ((lane & 1) == 0) {
-              const uint32_t word = pack_bf16x2(mine, next);  // low half = even column
-              if (lg) lg[(size_t)m * (a.W / 2) + wcol] = word;
-              const uint32_t y = word == kSentinel ? kSentAs : word;
-              const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + wcol;
-              if (r != a.skip_rank)
-                for (int d = 0; d < a.tp; ++d)
-                  st_relaxed_u32(reinterpret_cast<uint32_t*>(a.box[d]) + parity_off + off, y);
-            }
+            if ((lane & 1) == 0) stage[m * 16 + (lane >> 1)] = pack_bf16x2(mine, next);
           }
         }
+        __syncwarp();
+        const int grp = lane & 3;
+        // Word column of the group within rank r's row: tile t, this warp's 32
+        // rows (16 words), group grp (4 words).
+        const size_t wcol = (size_t)t * (kTileN / 2) + (size_t)quarter * 16 + (size_t)grp * 4;
+        const bool lg_vec = lg && (reinterpret_cast<uintptr_t>(lg) & 15) == 0;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          const int m = (lane >> 2) + pass * 8;
+          if (m < a.M) {
+            const uint4 x = *reinterpret_cast<const uint4*>(stage + m * 16 + grp * 4);
+            if (lg) {
+              uint32_t* dst = lg + (size_t)m * (a.W / 2) + wcol;
+              if (lg_vec) {
+                *reinterpret_cast<uint4*>(dst) = x;
+              } else {
+                dst[0] = x.x;
+                dst[1] = x.y;
+                dst[2] = x.z;
+                dst[3] = x.w;
+              }
+            }
+            uint4 y;
+            y.x = x.x == kSentinel ? kSentAs : x.x;
+            y.y = x.y == kSentinel ? kSentAs : x.y;
+            y.z = x.z == kSentinel ? kSentAs : x.z;
+            y.w = x.w == kSentinel ? kSentAs : x.w;
+            const size_t off = (size_t)m * (V / 2) + (size_t)r * (a.W / 2) + wcol;
+            if (r != a.skip_rank)
+              for (int d = 0; d < a.tp; ++d)
+                st_relaxed_v4(reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(a.box[d]) +
+                                                       parity_off + off),
+                              y);
+          }
+        }
+        __syncwarp();  // the next item rewrites the staged words
       }  // whole tile or part 0
       if (tl && warp == 2 && lane == 0 && i < kFusedTlPushN) tl[kFusedTlPush + i] = globaltimer_ns();
       // One item behind, the gather of the neighbour's tiles: its item i - 1
