@@ -133,6 +133,7 @@ struct Elem<uint32_t> {
 struct UnitPos {
   int r;       // source rank
   int idx;     // element index of slot 0 within the rank-row
+  int lim;     // end of the unit's elements within the rank-row (exclusive)
   size_t src;  // offset in rank r's shard
   size_t dst;  // offset in a mailbox parity and in an output
 };
@@ -144,9 +145,21 @@ __device__ __forceinline__ UnitPos unit_pos(const GatherArgs& a, int u, int lane
   const int rem = u - m * per_row;
   const int r = rem / a.chunks;
   const int c = rem - r * a.chunks;
+  // Chunk c covers elements [start, lim) of the rank-row: 32 * VPT elements
+  // from c * 32 * VPT (the last chunk ragged), or, with balanced chunks
+  // (a.chunk_q > 0), chunk_q elements, plus one for the first chunk_r chunks.
+  int start, lim;
+  if (a.chunk_q > 0) {
+    start = c * a.chunk_q + min(c, a.chunk_r);
+    lim = start + a.chunk_q + (c < a.chunk_r ? 1 : 0);
+  } else {
+    start = c * 32 * VPT;
+    lim = min(start + 32 * VPT, a.wv);
+  }
   UnitPos p;
   p.r = r;
-  p.idx = c * 32 * VPT + lane;
+  p.lim = lim;
+  p.idx = start + lane;
   p.src = (size_t)m * a.wv + p.idx;
   p.dst = (size_t)m * a.tp * a.wv + (size_t)r * a.wv + p.idx;
   return p;
@@ -183,7 +196,7 @@ __device__ __forceinline__ unsigned poll_begin(const GatherArgs& a, const V* box
   unsigned todo = 0;  // bit v: slot v still waits
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
-    if (p.idx + 32 * v < a.wv) todo |= 1u << v;
+    if (p.idx + 32 * v < p.lim) todo |= 1u << v;
   issue_polls<V, VPT>(box, p, todo, res);
   return todo;
 }
@@ -283,7 +296,7 @@ __device__ __forceinline__ void unit_stats(const GatherArgs& a, const UnitPos& p
   float m0 = kNegInf, m1 = kNegInf;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
-    const bool ok = p.idx + 32 * v < a.wv;
+    const bool ok = p.idx + 32 * v < p.lim;
 #pragma unroll
     for (int k = 0; k < E::kWords; ++k) {
       const uint32_t w = E::word(res[v], k);
@@ -299,7 +312,7 @@ __device__ __forceinline__ void unit_stats(const GatherArgs& a, const UnitPos& p
   float ls = 0.f;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
-    const bool ok = p.idx + 32 * v < a.wv;
+    const bool ok = p.idx + 32 * v < p.lim;
     const int col0 = p.r * a.shard_cols + (p.idx + 32 * v) * (2 * E::kWords);
 #pragma unroll
     for (int k = 0; k < E::kWords; ++k) {
@@ -456,7 +469,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
   // fewer in a ragged last chunk.
   if constexpr (sizeof(V) == 16) {
     if (a.l2_prefetch && threadIdx.x == 0 && push0 && p0.r != a.skip_rank) {
-      const int n = min(32 * VPT, a.wv - p0.idx);
+      const int n = p0.lim - p0.idx;  // from lane 0's first element
       if (n > 0)
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src0), "r"(n * 16)
                      : "memory");
@@ -495,7 +508,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
   if (push0 && p0.r != a.skip_rank) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
-      if (p0.idx + 32 * v < a.wv) x0[v] = E::ld_shard(src0 + 32 * v);
+      if (p0.idx + 32 * v < p0.lim) x0[v] = E::ld_shard(src0 + 32 * v);
   }
   // Device-resident parity: this warp's own copy (one load per warp of one
   // address, so every lane sees the same value).
@@ -515,7 +528,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
   if (push0 && p0.r != a.skip_rank) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
-      if (p0.idx + 32 * v < a.wv) E::st_relaxed(box + p0.dst + 32 * v, E::rewrite(x0[v]));
+      if (p0.idx + 32 * v < p0.lim) E::st_relaxed(box + p0.dst + 32 * v, E::rewrite(x0[v]));
   }
 
   // Shard loads of a push: with PREF issued one iteration ahead (during the
@@ -535,7 +548,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
     const V* src = reinterpret_cast<const V*>(a.shard[pn.r]) + pn.src;
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
-      if (pn.idx + 32 * v < a.wv) xn[v] = E::ld_shard(src + 32 * v);
+      if (pn.idx + 32 * v < pn.lim) xn[v] = E::ld_shard(src + 32 * v);
   };
   if (PREF) load_push(1);
 
@@ -544,7 +557,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
     if (pushn) {
 #pragma unroll
       for (int v = 0; v < VPT; ++v)
-        if (pn.idx + 32 * v < a.wv) E::st_relaxed(box + pn.dst + 32 * v, E::rewrite(xn[v]));
+        if (pn.idx + 32 * v < pn.lim) E::st_relaxed(box + pn.dst + 32 * v, E::rewrite(xn[v]));
       // Statistics are folded where the values already sit in registers: at
       // the push. Every warp pushes the same unit (into its own rank's
       // mailbox), so the fold of iteration t's push goes to warp t mod tp and
@@ -573,7 +586,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
       if (kTlStats && tl_here) a.timeline[(size_t)g * kTimelineSlots + 2 + 8] = globaltimer_ns();
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
-        if (p.idx + 32 * v < a.wv) {
+        if (p.idx + 32 * v < p.lim) {
           E::st_out(out + p.dst + 32 * v, res[v]);
           E::st_relaxed(box + p.dst + 32 * v, E::sentinel());
         }

@@ -45,7 +45,13 @@ struct GatherArgs {
   int tp;
   int wv;         // elements per rank-row
   int M;          // rows of this call
-  int chunks;     // units per rank-row: ceil(wv / (32 * vpt))
+  int chunks;     // units per rank-row: ceil(wv / (32 * vpt)), or a balanced count
+  // Balanced chunks (chunk_q > 0): chunk c of a rank-row holds chunk_q
+  // elements, plus one for c < chunk_r (chunk_q = wv / chunks, chunk_r = wv %
+  // chunks), at most 32 * vpt; chunk_q = 0: chunks of 32 * vpt elements, the
+  // last one ragged.
+  int chunk_q = 0;
+  int chunk_r = 0;
   int skip_rank;  // test hook: rank whose push is skipped (-1: none)
   // Device-resident parity: nullptr when box[] already points at the parity in
   // use. Otherwise box[] points at parity 0, parity p adds p * parity_stride
@@ -89,6 +95,7 @@ struct LaunchShape {
   bool late = false;   // trigger the next launch late (see trigger_late)
   bool timeline = false;  // the kernel writes a timeline record (16-byte vector
                           // path, tp <= 16, no prefetch)
+  bool balanced = false;  // balanced chunks (GatherArgs::chunk_q); tuner candidates only
 };
 
 // The kernel indexes units with int: a CTA's push index t * G + g runs up to

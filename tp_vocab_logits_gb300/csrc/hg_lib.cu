@@ -376,6 +376,10 @@ int gather_impl(hg_handle* h, const void* const* shard_ptrs, void* const* out_pt
   a.wv = h->wv;
   a.M = M;
   a.chunks = stats ? h->chunks_stats[M] : h->chunks[M];
+  if ((stats ? h->shape_stats[M] : h->shape[M]).balanced) {
+    a.chunk_q = h->wv / a.chunks;
+    a.chunk_r = h->wv % a.chunks;
+  }
   a.skip_rank = h->skip_rank;
   a.l2_prefetch = device_shards ? 1 : 0;
   if (stats) {
@@ -439,6 +443,23 @@ int tune_candidates(hg_handle* h, int M, const hg_options* opt, std::vector<Cand
         c.s.ctas = (int)g;
         c.s.late = hg::trigger_late(g, units, maxg);
         out->push_back(c);
+      }
+      // Balanced chunks (one wave, no prefetch, grid not forced): the chunk
+      // counts, up to twice the fixed one, for which the units fill a whole
+      // number of CTAs per SM, each chunk within 32 * vpt elements. With fixed
+      // chunks the grid can leave some SMs with one CTA more than others.
+      if (!pref && !opt->ctas) {
+        for (long long cc = c.chunks + 1; cc <= 2LL * c.chunks; ++cc) {
+          const long long u = (long long)M * h->tp * cc;
+          if (u > maxg) break;
+          if (u % h->sms != 0 || h->wv / cc < 1) continue;
+          Candidate b = c;
+          b.chunks = (int)cc;
+          b.s.balanced = true;
+          b.s.ctas = (int)u;
+          b.s.late = hg::trigger_late(u, u, maxg);
+          out->push_back(b);
+        }
       }
     }
   }
@@ -549,7 +570,8 @@ int autotune_shapes(hg_handle* h, const hg_options* opt) {
     const Candidate* rule = nullptr;
     for (const Candidate& c : cand) {
       if (c.us < fastest->us) fastest = &c;
-      if (c.s.vpt == fixed.s.vpt && c.s.ctas == fixed.s.ctas && c.s.pref == fixed.s.pref)
+      if (c.s.vpt == fixed.s.vpt && c.s.ctas == fixed.s.ctas && c.s.pref == fixed.s.pref &&
+          c.s.balanced == fixed.s.balanced)
         rule = &c;
     }
     const Candidate* best =
