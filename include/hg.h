@@ -418,7 +418,7 @@ typedef struct hg_row_stats {
 
 /*
  * hg_gather_stats - hg_gather plus sampler statistics of every gathered row,
- * folded by the pollers while they copy. The API page's module docstring
+ * folded where each unit is pushed and reduced per row inside the same kernel. The API page's module docstring
  * notes that the sentinel rewrite leaves every value a sampler uses
  * unchanged, so these are the sampler's statistics of the gathered row. Same
  * arguments, contract and errors as hg_gather (tp <= 16), plus
