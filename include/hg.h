@@ -251,7 +251,10 @@ int hg_launch_shape(const hg_handle *h, int M, int *ctas, int *threads, int *ele
  * warps of CTAs that gave up record nothing); for tp <= 14, warp_done[14]
  * holds instead the index of the SM the CTA ran on. In hg_gather_stats calls with
  * tp < 16, warp_done[15] holds when warp 0 finished its share of the gather
- * and turned to reducing the statistics of its rows. hg_gather_fused calls
+ * and turned to reducing the statistics of its rows, and for tp <= 8 warp 0
+ * also records in warp_done[8..12]: its first poll complete, its first
+ * outputs stored, its first unit folded, and (CTAs g < M, reducing row g) all
+ * of row g's cells arrived and folded, and row g's statistics written. hg_gather_fused calls
  * (one CTA per SM; recorded when the handle's grid records have room for it)
  * use the same slots differently: entry; set-up done (tensor memory and
  * barriers ready); warp_done[i] (i < 8): the epilogue has pushed its item i;

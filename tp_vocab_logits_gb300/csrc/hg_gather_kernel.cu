@@ -341,14 +341,18 @@ __device__ __forceinline__ void unit_stats(const GatherArgs& a, const UnitPos& p
 }
 
 // Warp 0 of CTA g, once its own units are done: for rows g, g + G, ..., poll
-// the row's cells until all have arrived (bounded), fold them, re-arm them and
-// write the row's statistics. BATCH cells per lane are in flight at once, so a
-// row of up to 32 * BATCH cells costs one wait. Rows are reduced by different
-// CTAs in parallel.
-// Only warps 0 write cells, and a reducer waits on cells that consumers write
-// without ever waiting on a reducer, so neither a CTA barrier nor any atomic is
-// involved: the cells carry their own arrival, as mailbox words do.
-template <int BATCH>
+// the row's cells until all have arrived (bounded), fold them, write the row's
+// statistics and re-arm the cells. BATCH cells per lane are in flight at once,
+// so a row of up to 32 * BATCH cells costs one wait. Rows are reduced by
+// different CTAs in parallel.
+// A cell is written once per call, by the warp that folded its unit, and a
+// reducer waits on cells without anyone ever waiting on a reducer, so neither
+// a CTA barrier nor any atomic is involved: the cells carry their own
+// arrival, as mailbox words do.
+// TL: lane 0 also records, for the first row, when all its cells had arrived
+// and been folded across the warp, and when its statistics were written
+// (timeline slots of warps 11 and 12, tp <= 8).
+template <int BATCH, bool TL>
 __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) {
   const int lane = (int)threadIdx.x & 31;
   const int per_row = a.tp * a.chunks;  // cells (units) per row
@@ -412,14 +416,23 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
         const float e = __expf(km[k] - bm);
         bs += (km[k] != kNegInf) ? __uint_as_float(v[k].z) * e : 0.f;
         ba = ((valid >> k & 1) && km[k] == bm) ? min(ba, (int)v[k].y) : ba;
-        if (valid >> k & 1) Elem<uint4>::st_relaxed(q + base + 32 * k, armed);
       }
-      combine_partial(mx, arg, s, bm, ba, bs);
+      if (base == lane) {  // the first batch (the only one up to 32 * BATCH cells)
+        mx = bm;
+        arg = ba;
+        s = bs;
+      } else {
+        combine_partial(mx, arg, s, bm, ba, bs);
+      }
     }
     float rm, rs;
     int ra;
     warp_stats(mx, arg, s, rm, ra, rs);
     if (__any_sync(kFull, gave_up)) return;
+    if constexpr (TL) {
+      if (m == g && lane == 0 && a.tp <= 8)
+        a.timeline[(size_t)g * kTimelineSlots + 2 + 11] = globaltimer_ns();
+    }
     if (lane == 0) {
       hg_row_stats r;
       r.max_logit = rm;
@@ -427,7 +440,13 @@ __device__ __forceinline__ void finish_stats(const GatherArgs& a, int g, int G) 
       r.sum_exp = rs;
       r.logsumexp = rm + logf(rs);
       a.stats[m] = r;
+      if constexpr (TL) {
+        if (m == g && a.tp <= 8) a.timeline[(size_t)g * kTimelineSlots + 2 + 12] = globaltimer_ns();
+      }
     }
+    // Re-arm the row's cells once its statistics are written: stored inside
+    // the fold, the re-arms held the fold back (0.3 us per call at one row).
+    for (int c = lane; c < per_row; c += 32) Elem<uint4>::st_relaxed(q + c, armed);
   }
 }
 
@@ -622,7 +641,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs& a) {
     if (d == 0 && lane == 0 && a.tp < 16)
       a.timeline[(size_t)g * kTimelineSlots + 2 + 15] = globaltimer_ns();
   }
-  if (STATS && d == 0 && g < a.M) finish_stats<(VPT <= 4 ? 8 : 6)>(a, g, G);
+  if (STATS && d == 0 && g < a.M) finish_stats<(VPT <= 4 ? 8 : 6), TL>(a, g, G);
   if constexpr (TL) {
     if (lane == 0) a.timeline[(size_t)g * kTimelineSlots + 2 + d] = globaltimer_ns();
   }
