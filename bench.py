@@ -764,6 +764,11 @@ def run_ours(args):
     staged_ms = time_calls(torch, [staged_step], args.steps, args.warmup, stream, "timed_staged")
     hg.hg_sync(h)
     staged_us = round(staged_ms * 1000.0 / args.steps, 3)
+    # the host link's write rate for the same bytes: the copy engine moving all
+    # ranks' outputs (TP * M * V bf16) to pinned host memory, nothing else
+    d2h_ms = time_calls(torch, [lambda: host_out1.copy_(dev_out, non_blocking=True)],
+                        args.steps, args.warmup, stream, "timed_d2h")
+    d2h_us = round(d2h_ms * 1000.0 / args.steps, 3)
     del host_in, host_out1, dev_in, dev_out
     e2e_ms_max, e2e_us = replica_us_per_call(dist, e2e_ms, args.steps, world, device)
     h.close()
@@ -890,7 +895,11 @@ def run_ours(args):
                         "written by the gather kernel itself over the host-device link",
                 "staged_copies_us_per_call": staged_us,
                 "one_result_copy_to_host_us_per_call": one_us,
-                "one_result_copy_d2h_bytes_per_step": M_STEP * V * 2},
+                "one_result_copy_d2h_bytes_per_step": M_STEP * V * 2,
+                "d2h_copy_of_outputs_alone_us": d2h_us,
+                "host_link_note": "d2h_copy_of_outputs_alone_us: the copy engine writing the "
+                                  "same d2h bytes to pinned host memory and nothing else; the "
+                                  "gather's e2e is bound by that write rate"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                      "traffic": traffic,

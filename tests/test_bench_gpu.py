@@ -38,6 +38,7 @@ def test_bench_line_carries_the_contract_keys():
     assert e["value"] > 0 and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 8 * 20480 * 2          # every rank's [1, W] shard
     assert e["d2h_bytes_per_step"] == 8 * 8 * 20480 * 2      # every rank's [1, V] row
+    assert e["d2h_copy_of_outputs_alone_us"] > 0              # the host link's write rate
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
