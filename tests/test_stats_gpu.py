@@ -1,4 +1,5 @@
-"""Sampler statistics folded into the gather's pollers (hg_gather_stats).
+"""Sampler statistics of the gathered rows (hg_gather_stats): each unit folded
+where it is pushed, the cells reduced per row in the same kernel.
 
 Per gathered row: max_logit and argmax must equal the oracle exactly (the max
 of bf16 values is exact in fp32, and both sides resolve ties to the smallest
@@ -115,4 +116,52 @@ def test_stats_interleaved_with_plain_gathers():
             hg.hg_gather(h, to_dev(bits), outs, M)
             hg.hg_sync(h)
             np.testing.assert_array_equal(from_dev(outs), want)
+    h.close()
+
+
+@pytest.mark.parametrize("device_parity", [False, True])
+def test_stats_back_to_back_random_rows(device_parity):
+    """A stream of 1,500 calls with a seeded sequence of row counts, two in
+    three with statistics and one in three plain, on one handle, synchronised
+    every 64 calls: every output row and every statistics row against the
+    oracle. Consecutive calls reuse each cell and mailbox row across parities
+    and shapes, which is where a missing re-arm or a cell read too early would
+    show."""
+    tp, W, cap, n_calls, ring = 8, 20480, 8, 1500, 64
+    h = hg.hg_create(tp, W, cap, device_parity=device_parity)
+    sets, want_dev, want_stats = [], [], []
+    for i in range(8):
+        bits = synth.shards(92, tp, cap, W, scale=3.0, sent_frac=0.01, set_index=i) \
+            .numpy().view(np.uint16)
+        want = oracle.Gather(tp, W, cap).call(bits)
+        sets.append(to_dev(bits))
+        want_dev.append(torch.from_numpy(want[0].view(np.int16).copy()).cuda())
+        want_stats.append([oracle.row_stats(want[0][m]) for m in range(cap)])
+    outs = [empty_outs(tp, cap, tp * W) for _ in range(ring)]
+    stats = [hg.new_row_stats(cap) for _ in range(ring)]
+    Ms = synth.row_sequence(11 + device_parity, n_calls, list(range(1, cap + 1)))
+    pend = []
+    for i, M in enumerate(Ms):
+        s_, o, st = i % len(sets), outs[i % ring], stats[i % ring]
+        with_stats = i % 3 != 2
+        shards = [x[:M] for x in sets[s_]]
+        if with_stats:
+            hg.hg_gather_stats(h, shards, [x[:M] for x in o], st[:M], M)
+        else:
+            hg.hg_gather(h, shards, [x[:M] for x in o], M)
+        pend.append((i, s_, M, with_stats))
+        if len(pend) == ring or i == n_calls - 1:
+            hg.hg_sync(h)
+            for j, sj, Mj, ws in pend:
+                for d in range(tp):
+                    assert torch.equal(outs[j % ring][d][:Mj], want_dev[sj][:Mj]), (j, d, Mj)
+                if ws:
+                    got = {k: v.cpu().numpy() for k, v in
+                           hg.unpack_row_stats(stats[j % ring][:Mj]).items()}
+                    for m in range(Mj):
+                        mx, arg, se = want_stats[sj][m]
+                        assert got["max_logit"][m] == mx and got["argmax"][m] == arg, (j, m)
+                        assert abs(got["sum_exp"][m] - se) <= 1e-4 * se, (j, m)
+            pend = []
+    assert_mailboxes_armed(h, hg)
     h.close()
