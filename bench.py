@@ -1159,7 +1159,7 @@ def run_fused_timeline(args):
     lib = hg.load()
     wp = (ctypes.c_void_p * tp)(*[w.data_ptr() for w in weight])
     for M in [int(x) for x in args.timeline_ms.split(",")]:
-        h = hg.hg_create(tp, Wd, 8, rows=[1, 4, 8], timeline_calls=n)
+        h = hg.hg_create(tp, Wd, max(8, M), rows=sorted({1, 4, 8, M}), timeline_calls=n)
         hid = synth.hidden(4, tp, M, K, device=device)
         outs = torch.empty((tp, M, tp * Wd), dtype=torch.int16, device=device)
         hp = (ctypes.c_void_p * tp)(*[hid[r].data_ptr() for r in range(tp)])
