@@ -97,8 +97,9 @@ int max_grid(const hg_handle* h, const hg::LaunchShape& s, long long* g) {
 // Launch shape for M rows by the fixed rule, unless the options force part of
 // it: one CTA = one warp per virtual rank; each lane carries default_vpt(tp, M)
 // elements (3 for up to three rows at tp <= 8, 4 otherwise, 2 for CTAs of 1024
-// threads; the statistics kernel: stats_vpt); one CTA per unit up to the
-// co-resident maximum, beyond which the CTAs loop over the units; no prefetch.
+// threads; the statistics kernel: stats_vpt), widened when a small remainder
+// would spill past one wave (below); one CTA per unit up to the co-resident
+// maximum, beyond which the CTAs loop over the units; no prefetch.
 // The best shape depends on tp, W and M in ways no simple rule captures, so
 // hg_options.autotune can time the candidates instead. The grid never exceeds
 // the co-resident CTA count, which the kernel's cross-CTA polls need.
@@ -128,6 +129,34 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchS
   s.late = hg::trigger_late(G, units, maxg);
   *out = s;
   *chunks_out = chunks;
+  // A small remainder past one wave (at most a tenth of the grid): wider
+  // units may fit every unit in one wave. Take them if they leave the
+  // heaviest SM fewer vectors to move (CTAs spread evenly over the SMs; the
+  // remainder's units land on different SMs). TP8, V=163840, M=4: 640 units
+  // of 128 vectors on 608 CTAs (heaviest SM: 5 units, 640 vectors) took
+  // 6.07-6.11 us; 448 units of 192 on 448 CTAs (3 units, 576 vectors) 5.88
+  // us; 512 of 160 (4 units, 640 vectors) 6.11 us. At M=3 the same count keeps
+  // 3 elements per lane (480 vectors, against 480 and 512).
+  if (!stats && !forced_vpt && !forced_ctas && units > maxg && units * 10 <= maxg * 11) {
+    const long long sms = h->sms;
+    long long best = ((G + sms - 1) / sms + (units - G + sms - 1) / sms) * 32LL * s.vpt;
+    for (int v = s.vpt + 1; v <= hg::max_vpt(h->tp); ++v) {
+      hg::LaunchShape c = s;
+      c.vpt = v;
+      const int cv = (h->wv + 32 * v - 1) / (32 * v);
+      const long long uv = (long long)M * h->tp * cv;
+      long long mv = 0;
+      if (max_grid(h, c, &mv) != HG_OK || uv > mv) continue;
+      const long long heavy = (uv + sms - 1) / sms * 32LL * v;
+      if (heavy < best) {
+        best = heavy;
+        c.ctas = (int)uv;
+        c.late = hg::trigger_late(uv, uv, mv);
+        *out = c;
+        *chunks_out = cv;
+      }
+    }
+  }
   return HG_OK;
 }
 
