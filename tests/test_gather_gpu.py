@@ -434,11 +434,12 @@ def test_create_rejects_bad_sizes():
     with pytest.raises(hg.HGError):
         hg.hg_create(24, 64, 4, elems_per_lane=3)  # 1024-thread CTAs: 1 or 2 per lane
     h = hg.hg_create(8, 20480, 8)
-    # M=4 at 4 per lane would leave 32 of 640 units past one wave: 6 per lane
-    # fits all 448 units in one wave with fewer vectors on the heaviest SM
-    shapes = [hg.hg_launch_shape(h, M) for M in (1, 2, 3, 4, 8)]
-    assert [s["elems_per_lane"] for s in shapes] == [3, 3, 3, 6, 4]
-    assert [s["ctas"] for s in shapes] == [216, 432, 608, 448, 608]
+    # from four rows on, the width whose busiest SM moves the fewest vectors:
+    # M=4 6 per lane (576 against 640), M=5 and M=6 4, M=7 and M=8 5
+    Ms = (1, 2, 3, 4, 5, 6, 7, 8)
+    shapes = [hg.hg_launch_shape(h, M) for M in Ms]
+    assert [s["elems_per_lane"] for s in shapes] == [3, 3, 3, 6, 4, 4, 5, 5]
+    assert [s["ctas"] for s in shapes] == [216, 432, 608, 448, 608, 608, 608, 608]
     h.close()
     h = hg.hg_create(16, 4096, 2)
     assert hg.hg_launch_shape(h, 1)["elems_per_lane"] == 4
