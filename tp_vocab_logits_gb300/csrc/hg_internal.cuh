@@ -136,7 +136,8 @@ inline int default_vpt(int tp, int M) {
 // eight rows at tp <= 8, where the smaller units shorten each unit's fold and
 // the reducer still polls a row's cells in one wait; 4 otherwise. (TP8,
 // V=163840, M=1: 3.79 us graph-replayed, against 3.91 / 4.24 / 4.80 us with 4 /
-// 5 / 6 elements per lane and 4.46 us with 2.)
+// 5 / 6 elements per lane and 4.46 us with 2; M=8: 10.87 us against 11.15 / 11.51
+// with 4 / 5; M=7: 9.84 against 10.10 / 10.42 / 12.08 with 4 / 5 / 6.)
 inline int stats_vpt(int tp, int M) { return (tp <= 8 && M <= 8) ? 3 : 4; }
 
 // Largest co-resident CTAs per SM of the gather kernel for this shape.
