@@ -441,6 +441,13 @@ def test_create_rejects_bad_sizes():
     assert [s["elems_per_lane"] for s in shapes] == [3, 3, 3, 6, 4, 4, 5, 5]
     assert [s["ctas"] for s in shapes] == [216, 432, 608, 448, 608, 608, 608, 608]
     h.close()
+    # the same count on other shapes of the bandwidth sweep (each measured faster):
+    # TP4 W=20480 M=8 6 per lane on 448 CTAs, TP2 W=20480 M=32 5 per lane
+    for tp, W, M, want in [(4, 20480, 8, (448, 6)), (2, 20480, 32, (1024, 5))]:
+        h = hg.hg_create(tp, W, M, rows=[M])
+        s = hg.hg_launch_shape(h, M)
+        assert (s["ctas"], s["elems_per_lane"]) == want, (tp, W, M, s)
+        h.close()
     h = hg.hg_create(16, 4096, 2)
     assert hg.hg_launch_shape(h, 1)["elems_per_lane"] == 4
     h.close()
