@@ -143,6 +143,12 @@ inline int stats_vpt(int tp, int M) { return (tp <= 8 && M <= 8) ? 3 : 4; }
 // Largest co-resident CTAs per SM of the gather kernel for this shape.
 cudaError_t gather_occupancy(const LaunchShape& s, bool vec16, int tp, int* ctas_per_sm);
 
+// The fixed rule's unit widening (hg_lib.cu): from four rows on, for launches
+// of at most four rounds, replace *s (the default width's shape: vpt, ctas,
+// late) and *chunks with the width whose busiest SM moves the fewest vectors.
+cudaError_t widen_units(int tp, int wv, int M, int sms, bool vec16, LaunchShape* s,
+                        int* chunks);
+
 // Launch of the gather kernel. cooperative: the runtime guarantees that all
 // CTAs are co-resident (or fails the launch); otherwise a programmatic
 // dependent launch (the kernel waits for its predecessor before any access).

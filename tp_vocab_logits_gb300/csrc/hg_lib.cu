@@ -51,6 +51,66 @@ struct hg_handle {
   long long timeline_next = 0;      // calls recorded so far
 };
 
+namespace hg {
+
+// From four rows on, where the call moves enough bytes that the busiest SM
+// sets its time, wider units may load that SM with fewer vectors: CTA i
+// takes units i, i + G, ..., and SM j holds CTAs j, j + S, ... (the launch
+// spreads CTAs over the SMs in turn). Take the width whose busiest SM moves
+// the fewest vectors (ties keep the narrower), for launches of at most four
+// rounds. TP8, V=163840, graph-replayed: M=4 6 per lane on 448 CTAs (576
+// vectors on the busiest SM against 640 with 4) 5.88 against 6.07-6.11 us;
+// M=7 5 per lane (960 against 1024) 9.11 against 9.53-9.56 us; M=8 5 per
+// lane (1120 against 1152) 10.36-10.37 against 10.49-10.52 us; M=5 and M=6
+// keep 4 (768 and 896, against 800 and 960 with 5: 7.42 and 8.23 against
+// 7.01-7.03 and 8.02-8.04 us). Past four rounds five of six sweep points got
+// slower. Up to three rows at tp <= 8 the chain of vectors per lane sets the
+// time instead, and the narrow rule stays.
+cudaError_t widen_units(int tp, int wv, int M, int sms, bool vec16, LaunchShape* s,
+                        int* chunks) {
+  if (M < 4) return cudaSuccess;
+  int per_sm = 0;
+  cudaError_t e = gather_occupancy(*s, vec16, tp, &per_sm);
+  if (e != cudaSuccess) return e;
+  const long long S = sms;
+  const long long maxg = (long long)per_sm * S;
+  const long long units = (long long)M * tp * *chunks;
+  if (per_sm < 1 || units > 4 * maxg) return cudaSuccess;
+  auto busiest = [S](long long U, long long Gc, int v) {
+    long long worst = 0;
+    for (long long j = 0; j < S && j < Gc; ++j) {
+      long long load = 0;
+      for (long long i = j; i < Gc; i += S) load += (U - 1 - i) / Gc + 1;
+      if (load > worst) worst = load;
+    }
+    return worst * 32LL * v;
+  };
+  long long best = busiest(units, units < maxg ? units : maxg, s->vpt);
+  const LaunchShape base = *s;
+  for (int v = base.vpt + 1; v <= max_vpt(tp); ++v) {
+    LaunchShape c = base;
+    c.vpt = v;
+    int pv = 0;
+    if (gather_occupancy(c, vec16, tp, &pv) != cudaSuccess || pv < 1) continue;
+    const long long mv = (long long)pv * S;
+    const int cv = (wv + 32 * v - 1) / (32 * v);
+    const long long uv = (long long)M * tp * cv;
+    if (!units_fit_int(uv, mv)) continue;
+    const long long gv = uv < mv ? uv : mv;
+    const long long load = busiest(uv, gv, v);
+    if (load < best) {
+      best = load;
+      c.ctas = (int)gv;
+      c.late = trigger_late(gv, uv, mv);
+      *s = c;
+      *chunks = cv;
+    }
+  }
+  return cudaSuccess;
+}
+
+}  // namespace hg
+
 namespace {
 
 using hg::GatherArgs;
@@ -98,8 +158,9 @@ int max_grid(const hg_handle* h, const hg::LaunchShape& s, long long* g) {
 // it: one CTA = one warp per virtual rank; each lane carries default_vpt(tp, M)
 // elements (3 for up to three rows at tp <= 8, 4 otherwise, 2 for CTAs of 1024
 // threads; the statistics kernel: stats_vpt), widened from four rows on when
-// that leaves the busiest SM fewer vectors (below); one CTA per unit up to the
-// co-resident maximum, beyond which the CTAs loop over the units; no prefetch.
+// that leaves the busiest SM fewer vectors (widen_units); one CTA per unit up
+// to the co-resident maximum, beyond which the CTAs loop over the units; no
+// prefetch.
 // The best shape depends on tp, W and M in ways no simple rule captures, so
 // hg_options.autotune can time the candidates instead. The grid never exceeds
 // the co-resident CTA count, which the kernel's cross-CTA polls need.
@@ -129,48 +190,9 @@ int plan_one(hg_handle* h, int M, const hg_options* opt, bool stats, hg::LaunchS
   s.late = hg::trigger_late(G, units, maxg);
   *out = s;
   *chunks_out = chunks;
-  // From four rows on, where the call moves enough bytes that the busiest SM
-  // sets its time, wider units may load that SM with fewer vectors: CTA i
-  // takes units i, i + G, ..., and SM j holds CTAs j, j + S, ... (the launch
-  // spreads CTAs over the SMs in turn). Take the width whose busiest SM moves
-  // the fewest vectors (ties keep the narrower), for launches of at most four
-  // rounds. TP8, V=163840, graph-replayed: M=4 6 per lane on 448 CTAs (576
-  // vectors on the busiest SM against 640 with 4) 5.88 against 6.07-6.11 us;
-  // M=7 5 per lane (960 against 1024) 9.11 against 9.53-9.56 us; M=8 5 per
-  // lane (1120 against 1152) 10.36-10.37 against 10.49-10.52 us; M=5 and M=6
-  // keep 4 (768 and 896, against 800 and 960 with 5: 7.42 and 8.23 against
-  // 7.01-7.03 and 8.02-8.04 us). Up to three rows at tp <= 8 the chain of
-  // vectors per lane sets the time instead, and the narrow rule stays.
-  if (!stats && !forced_vpt && !forced_ctas && M >= 4 && units <= 4 * maxg) {
-    const long long S = h->sms;
-    auto busiest = [S](long long U, long long Gc, int v) {
-      long long worst = 0;
-      for (long long j = 0; j < S && j < Gc; ++j) {
-        long long load = 0;
-        for (long long i = j; i < Gc; i += S) load += (U - 1 - i) / Gc + 1;
-        if (load > worst) worst = load;
-      }
-      return worst * 32LL * v;
-    };
-    long long best = busiest(units, G, s.vpt);
-    for (int v = s.vpt + 1; v <= hg::max_vpt(h->tp); ++v) {
-      hg::LaunchShape c = s;
-      c.vpt = v;
-      const int cv = (h->wv + 32 * v - 1) / (32 * v);
-      const long long uv = (long long)M * h->tp * cv;
-      long long mv = 0;
-      if (max_grid(h, c, &mv) != HG_OK || !hg::units_fit_int(uv, mv)) continue;
-      const long long gv = uv < mv ? uv : mv;
-      const long long load = busiest(uv, gv, v);
-      if (load < best) {
-        best = load;
-        c.ctas = (int)gv;
-        c.late = hg::trigger_late(gv, uv, mv);
-        *out = c;
-        *chunks_out = cv;
-      }
-    }
-  }
+  if (!stats && !forced_vpt && !forced_ctas && !s.pref &&
+      hg::widen_units(h->tp, h->wv, M, h->sms, h->vec16, out, chunks_out) != cudaSuccess)
+    return HG_ERR_CUDA;
   return HG_OK;
 }
 

@@ -127,8 +127,9 @@ extern "C" int hg_gather_static(int tp, int shard_cols, const void* const* shard
   a.l2_prefetch = 1;
 
   // Launch shape: the library's fixed rule (elements per lane by tp and M,
-  // one CTA per unit up to the co-resident maximum, beyond which the CTAs
-  // loop over the units).
+  // widened from four rows on where that unloads the busiest SM; one CTA per
+  // unit up to the co-resident maximum, beyond which the CTAs loop over the
+  // units).
   hg::LaunchShape s;
   s.vpt = hg::default_vpt(tp, M);
   a.chunks = (wv + 32 * s.vpt - 1) / (32 * s.vpt);
@@ -138,6 +139,8 @@ extern "C" int hg_gather_static(int tp, int shard_cols, const void* const* shard
   const long long maxg = (long long)per_sm * ds.sms;
   s.ctas = (int)(units < maxg ? units : maxg);
   s.late = hg::trigger_late(s.ctas, units, maxg);
+  if (hg::widen_units(tp, wv, M, ds.sms, vec16, &s, &a.chunks) != cudaSuccess)
+    return HG_ERR_CUDA;
 
   // The array keeps the last call's contents: clear the status words and arm
   // this call's mailbox region, then gather, all in stream order.
