@@ -126,7 +126,7 @@ inline int max_vpt(int tp) { return tp <= 16 ? 6 : 2; }
 // CTAs in flight; 4 otherwise (2 for tp > 16, whose CTAs have 1024 threads).
 // Graph-replayed at TP8, V=163840, M=3: 4.88 us with 3 (608 CTAs) against 5.21
 // with 4 (480 CTAs). From four rows on the host may widen the units when that
-// leaves the busiest SM fewer vectors to move (plan_one).
+// leaves the busiest SM fewer vectors to move (widen_units).
 inline int default_vpt(int tp, int M) {
   if (tp > 16) return 2;
   return (tp <= 8 && M <= 3) ? 3 : 4;
